@@ -1,0 +1,238 @@
+"""Acceptance rules of one verify round (oracle; test infrastructure only).
+
+Layout of one round for sequence b (verify block, window width W = gamma + 1):
+row 0 holds the pending token (the last committed token, whose KV is not yet in
+the cache), rows 1..gamma hold the drafts x_1..x_gamma.  Row j's logits give the
+target distribution of the token after row j, so the draft x_i is tested
+against row i-1, and row gamma is the bonus distribution.
+
+Sources:
+* Greedy: "Per-step cost versus accepted tokens", section "What SGLang actually
+  runs" -- compare each draft with the target argmax at its position, take the
+  cumulative product of the matches; its sum is the accepted length; the round
+  commits the accepted drafts plus one target token.  Lecture 6 "Optimizing
+  Autoregressive Decode" section 7.4 -- at temperature 0 the rule reduces to
+  exactly this, and the output equals the target's own greedy decode.
+* Stochastic: Lecture 6 section 6.2 (Leviathan Algorithm 1): accept x_i while a
+  uniform r_i < p_i(x_i)/q_i(x_i), stop at the first rejection; after a
+  rejection at position n+1 draw from norm(max(0, p_{n+1} - q_{n+1})); after
+  full acceptance draw the bonus from p_{gamma+1}.  Section 7.1 proves the
+  output law equals p; section 7.2 gives P(accept) = sum min(p, q) = 1 - TV.
+* Tree: Lecture 6 section 10.3 -- one forward over a token tree under an
+  ancestor mask; greedy acceptance keeps the longest root-to-leaf path whose
+  tokens match the target argmax.
+
+Readings where the pages leave a step open (each is listed in the design doc):
+* The test r_i < p/q is evaluated as fl32(u * q(x)) < p(x): no division, the
+  same set of outcomes for q > 0; q(x) = 0 < p(x) accepts, p(x) = 0 rejects.
+* Uniforms u[b, 0..gamma-1] drive the tests, u[b, gamma] drives the one final
+  draw (residual or bonus); exactly one final draw happens per round.
+* The final draw is an integer inverse CDF (see `draw_index`) so that it is
+  reproducible bit for bit under any summation order.
+* Greedy ties go to the lowest token index.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+TWO_POW_40 = float(2 ** 40)
+TWO_POW_24 = float(2 ** 24)
+MASK24 = np.uint64((1 << 24) - 1)
+
+
+# ----------------------------------------------------------------------------- p
+def target_probs(logits: np.ndarray, temperature: float) -> np.ndarray:
+    """p = softmax(logits / T) over the last axis, in float64, rounded to float32.
+
+    Lecture 6 section 7.3: temperature sampling is sampling from softmax(logits/T).
+    """
+    z = np.asarray(logits, dtype=np.float64) / float(temperature)
+    z = z - z.max(axis=-1, keepdims=True)
+    e = np.exp(z)
+    return (e / e.sum(axis=-1, keepdims=True)).astype(np.float32)
+
+
+# ------------------------------------------------------------------- greedy chain
+def accept_greedy(logits: np.ndarray, x: np.ndarray):
+    """Greedy longest-matching-prefix acceptance.
+
+    logits [B, W, V] (any float), x [B, gamma] drafts.  Returns
+    (accepted [B], committed [B, W] with -1 after the first n+1 entries, bonus [B]).
+    """
+    logits = np.asarray(logits)
+    B, W, _ = logits.shape
+    gamma = W - 1
+    a = np.argmax(logits, axis=-1)                 # first maximal index on ties
+    match = (np.asarray(x).reshape(B, gamma) == a[:, :gamma]).astype(np.int64)
+    n = np.cumprod(match, axis=1).sum(axis=1) if gamma > 0 else np.zeros(B, np.int64)
+    bonus = a[np.arange(B), n]
+    committed = np.full((B, W), -1, dtype=np.int64)
+    for b in range(B):
+        committed[b, :n[b]] = x[b, :n[b]]
+        committed[b, n[b]] = bonus[b]
+    return n.astype(np.int64), committed, bonus.astype(np.int64)
+
+
+# ----------------------------------------------------------------- stochastic chain
+def accept_test(u: np.ndarray, q_x: np.ndarray, p_x: np.ndarray) -> np.ndarray:
+    """r < p/q evaluated as fl32(u * q) < p (float32, no fused multiply-add)."""
+    prod = np.multiply(np.float32(1.0) * u.astype(np.float32), q_x.astype(np.float32),
+                       dtype=np.float32)
+    return prod < p_x.astype(np.float32)
+
+
+def residual(p_row: np.ndarray, q_row: np.ndarray) -> np.ndarray:
+    """max(0, p - q) in float32 (unnormalised; the draw normalises)."""
+    return np.maximum(np.float32(0.0), (p_row.astype(np.float32) - q_row.astype(np.float32)))
+
+
+def fixed_point_mass(r: np.ndarray) -> np.ndarray:
+    """R_v = floor(r_v * 2^40) as uint64.  Exact: r is float32 <= 1."""
+    return np.floor(np.asarray(r, dtype=np.float32).astype(np.float64) * TWO_POW_40).astype(np.uint64)
+
+
+def draw_index(R: np.ndarray, u: float) -> int:
+    """Integer inverse-CDF draw from the unnormalised masses R (uint64, one row).
+
+    S = sum R, m = floor(u * 2^24), t = floor(m * S / 2^24); return the smallest
+    v with R_0 + ... + R_v > t.  P(v) = R_v / S up to the 2^-24 grid of u.
+    Returns -1 when S == 0.  Written with Python integers (no overflow).
+    """
+    S = int(np.sum(R, dtype=np.uint64))
+    if S == 0:
+        return -1
+    m = int(np.floor(np.float64(np.float32(u)) * TWO_POW_24))
+    t = (m * S) >> 24
+    c = np.cumsum(R, dtype=np.uint64)
+    return int(np.searchsorted(c, np.uint64(t), side="right"))
+
+
+def draw_index_rows(R: np.ndarray, u: np.ndarray) -> np.ndarray:
+    """`draw_index` for many rows at once: R [B, V] uint64, u [B] float32.
+
+    (m * S) >> 24 is formed without a 128-bit product through the identity
+    m*S = m*S_hi*2^24 + m*S_lo with S_hi = S >> 24, S_lo = S mod 2^24, so
+    (m*S) >> 24 = m*S_hi + ((m*S_lo) >> 24); both terms fit in 64 bits
+    because m < 2^24 and S < 2^58.
+    """
+    R = np.asarray(R, dtype=np.uint64)
+    S = R.sum(axis=1, dtype=np.uint64)
+    m = np.floor(np.asarray(u, dtype=np.float32).astype(np.float64) * TWO_POW_24).astype(np.uint64)
+    t = m * (S >> np.uint64(24)) + ((m * (S & MASK24)) >> np.uint64(24))
+    c = np.cumsum(R, axis=1, dtype=np.uint64)
+    idx = (c <= t[:, None]).sum(axis=1).astype(np.int64)
+    idx[S == 0] = -1
+    return idx
+
+
+def accept_stochastic(p: np.ndarray, q: np.ndarray, x: np.ndarray, u: np.ndarray,
+                      accept_fn=accept_test, residual_fn=residual):
+    """Chain rejection sampling (Leviathan Algorithm 1) for a batch of rounds.
+
+    p [B, W, V] float32 target probabilities (row j = p_{j+1}), q [B, gamma, V]
+    float32 draft probabilities (q[:, i-1] = q_i), x [B, gamma] drafts, u [B, W]
+    float32 uniforms.  gamma = 0 is a plain sample from p (the decode step).
+
+    Returns (accepted [B], committed [B, W] (-1 padded), final [B], zero_residual [B])
+    where zero_residual flags rounds whose residual had no mass on the 2^-40 grid;
+    those draw from p at the break row instead.
+    """
+    p = np.asarray(p, dtype=np.float32)
+    B, W, V = p.shape
+    gamma = W - 1
+    x = np.asarray(x, dtype=np.int64).reshape(B, gamma)
+    u = np.asarray(u, dtype=np.float32).reshape(B, W)
+    bi = np.arange(B)
+    n = np.zeros(B, dtype=np.int64)
+    alive = np.ones(B, dtype=bool)
+    for i in range(gamma):
+        xi = x[:, i]
+        ok = accept_fn(u[:, i], q[bi, i, xi], p[bi, i, xi])
+        alive &= ok
+        n += alive
+    rejected = n < gamma
+    r = p[bi, n].copy()                          # full acceptance: bonus from p_{gamma+1}
+    if gamma > 0 and rejected.any():
+        rb = bi[rejected]
+        r[rb] = residual_fn(p[rb, n[rb]], q[rb, n[rb]])
+    R = fixed_point_mass(r)
+    tok = draw_index_rows(R, u[:, gamma])
+    zero = tok < 0
+    if zero.any():
+        tok[zero] = draw_index_rows(fixed_point_mass(p[bi[zero], n[zero]]), u[zero, gamma])
+    committed = np.full((B, W), -1, dtype=np.int64)
+    for b in range(B):
+        committed[b, :n[b]] = x[b, :n[b]]
+        committed[b, n[b]] = tok[b]
+    return n, committed, tok, zero
+
+
+def accept_stochastic_from_logits(logits, q, x, u, temperature: float):
+    """The verify round's acceptance as the library runs it: p from the logits, then
+    `accept_stochastic`.  Also returns the margins of each decision."""
+    p = target_probs(logits, temperature)
+    return accept_stochastic(p, q, x, u), p
+
+
+# --------------------------------------------------------------------------- tree
+def tree_depths(parent: np.ndarray) -> np.ndarray:
+    """Depth of every node; parent[0] = -1 (root), parent[c] < c (BFS order)."""
+    parent = np.asarray(parent, dtype=np.int64)
+    depth = np.zeros(len(parent), dtype=np.int64)
+    for c in range(1, len(parent)):
+        assert 0 <= parent[c] < c, "nodes must be in BFS order with parent < child"
+        depth[c] = depth[parent[c]] + 1
+    return depth
+
+
+def tree_ancestors(parent: np.ndarray) -> list:
+    """For each node, the set of its ancestors including itself."""
+    parent = np.asarray(parent, dtype=np.int64)
+    anc = []
+    for c in range(len(parent)):
+        s = {c}
+        v = c
+        while parent[v] >= 0:
+            v = int(parent[v])
+            s.add(v)
+        anc.append(s)
+    return anc
+
+
+def accept_tree_greedy(logits: np.ndarray, tok: np.ndarray, parent: np.ndarray):
+    """Greedy walk of a token tree: from the root, move to the child whose token is
+    the target argmax at the current node (lowest node index if several), stop when
+    none matches; the argmax at the stopping node is the bonus token.
+
+    logits [B, N, V], tok [B, N] (node 0 = pending token), parent [N].
+    Returns (accepted [B], path [B, maxdepth] node ids (-1 padded),
+             committed [B, maxdepth+1] tokens (-1 padded), bonus [B]).
+    """
+    logits = np.asarray(logits)
+    B, N, _ = logits.shape
+    parent = np.asarray(parent, dtype=np.int64)
+    depth = tree_depths(parent)
+    dmax = int(depth.max())
+    accepted = np.zeros(B, dtype=np.int64)
+    path = np.full((B, max(dmax, 1)), -1, dtype=np.int64)
+    committed = np.full((B, dmax + 1), -1, dtype=np.int64)
+    bonus = np.zeros(B, dtype=np.int64)
+    for b in range(B):
+        v, k = 0, 0
+        while True:
+            a = int(np.argmax(logits[b, v]))
+            nxt = -1
+            for c in range(1, N):
+                if parent[c] == v and int(tok[b, c]) == a:
+                    nxt = c
+                    break
+            if nxt < 0:
+                break
+            path[b, k] = nxt
+            committed[b, k] = a
+            k += 1
+            v = nxt
+        accepted[b] = k
+        committed[b, k] = a
+        bonus[b] = a
+    return accepted, path, committed, bonus
