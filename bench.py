@@ -1,0 +1,569 @@
+#!/usr/bin/env python
+"""Benchmark of the speculative-decoding verify round on GB300.
+
+Workload (default): Llama-3.1-8B-shaped target (32 layers, d 4096, 32 q / 8 kv
+heads of 128, ffn 14336, vocab 128256), random-init N(0, 0.02) bf16 weights,
+B = 1 sequence with 1024 cached tokens of random-token prompt in paged KV (page
+64), gamma = 4 drafts per round (verify width 5), drafts x_i ~ q_i =
+(1 - lam) p_i + lam Dir(1) with lam = 0.5 and p_i the target at the draft prefix,
+sampled acceptance at temperature 1.
+
+A step is one whole verify round through the C ABI (spec_verify_step): embed,
+32 decoder layers (fused QKV, RoPE + paged KV write, paged attention, O, gate/up
++ SwiGLU, down), final norm + LM head, softmax statistics, accept / resample /
+bonus, KV commit.  The weights (15 GB) are far larger than L2, so every step
+streams them from HBM; no L2 flush is needed.
+
+Rounds are first run for real (untimed) to build each round's drafts from the
+target's own p at the draft prefix; the cache is then rebuilt and the recorded
+rounds are replayed inside the timed region (the replay reproduces the same
+accepted counts bit for bit, which is checked).
+
+Also reported: e2e (the same rounds with host-resident inputs/outputs copied
+inside the timed region), the per-kernel roofline from a separate profiling
+pass, T_verify/T_decode for verify widths 1..8, and the CPU oracle timed on a
+bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "accepted tok/s at Llama-8B shape; T_verify/T_decode for gamma+1=2..8; HBM GB/s"
+UNIT = "accepted tok/s"
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--batch", type=int, default=1)
+    ap.add_argument("--ctx", type=int, default=1024)
+    ap.add_argument("--gamma", type=int, default=4)
+    ap.add_argument("--lam", type=float, default=0.5)
+    ap.add_argument("--temperature", type=float, default=1.0)
+    ap.add_argument("--layers", type=int, default=32, help="decoder layers (32 = the full 8B shape)")
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-lam-sweep", action="store_true")
+    ap.add_argument("--cpu-layers", type=int, default=2, help="layers in the oracle's timed sample")
+    ap.add_argument("--quick", action="store_true", help="a short run for profilers: timed replay only")
+    return ap.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")), \
+        int(os.environ.get("WORLD_SIZE", "1"))
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, local_rank: int):
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        ids = [v.strip() for v in vis.split(",")] if vis else []
+        self.gpu_index = ids[local_rank] if local_rank < len(ids) else str(local_rank)
+        self.proc = None
+        self.path = os.path.join("/tmp", f"spec_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.gpu_index), "-lms", "100"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]), util=float(parts[4]),
+                                 hw=parts[6], hwt=parts[7], swt=parts[8], pc=parts[9]))
+            except ValueError:
+                continue
+        load = [r for r in rows if r["util"] >= 50] or rows
+        if not load:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        reasons = set()
+        for r in load:
+            for k, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"), ("swt", "sw_thermal_slowdown"),
+                            ("pc", "sw_power_cap")):
+                if r[k].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in load), "sm_max_mhz": max(r["smax"] for r in load),
+                "reasons": sorted(reasons), "samples": len(load)}
+
+
+# ---------------------------------------------------------------- our arm
+class Bench:
+    def __init__(self, args, device):
+        import torch
+
+        from speculative_decoding_verify_step_gb300 import spec, synth
+        self.torch, self.spec, self.synth = torch, spec, synth
+        self.args = args
+        self.dev = device
+        self.dims = synth.LLAMA8B.with_layers(args.layers)
+        B, ctx = args.batch, args.ctx
+        self.B = B
+        self.max_seq = ctx + 64 * 32
+        pages_per_seq = -(-self.max_seq // 64)
+        self.model = spec.SpecModel(self.dims, max_batch=B, max_width=16, max_seq_len=self.max_seq,
+                                    num_pages=B * pages_per_seq + 8)
+        self.model.load_weights(synth.iter_weights(self.dims, seed=1, device=device))
+        torch.cuda.synchronize()
+        self.ids = torch.arange(B, dtype=torch.int32, device=device)
+        self.prompts = synth.prompts(B, ctx + 1, self.dims.vocab, seed=2).to(device)
+        self.stream = torch.cuda.current_stream()
+
+    def reset(self):
+        B = self.B
+        self.model.seq_reset(list(range(B)))
+        self.model.prefill(self.ids, self.prompts, [self.args.ctx + 1] * B)
+        self.model.sync_status()
+        return self.prompts[:, -1].clone()
+
+    # -------------------------------------------------------- record rounds
+    def record(self, n_rounds, gamma, lam, temp, seed):
+        torch = self.torch
+        B, V = self.B, self.dims.vocab
+        pending = self.reset()
+        gen = torch.Generator(device=self.dev)
+        gen.manual_seed(seed)
+        rounds, accepted = [], []
+        for r in range(n_rounds):
+            tok = torch.empty(B, gamma + 1, dtype=torch.int32, device=self.dev)
+            tok[:, 0] = pending
+            q = torch.empty(B, gamma, V, dtype=torch.float32, device=self.dev)
+            D = self.synth.dirichlet1((B, gamma, V), seed=seed * 1000 + r, device=self.dev)
+            for i in range(1, gamma + 1):
+                logits = self.model.score(self.ids, tok[:, :i])[:, i - 1].double()
+                p = torch.softmax(logits / temp, dim=-1)
+                qi = (1 - lam) * p + lam * D[:, i - 1]
+                q[:, i - 1] = qi.float()
+                tok[:, i] = torch.multinomial(qi, 1, generator=gen)[:, 0].int()
+            u = self.synth.uniforms((B, gamma + 1), seed=seed * 1000 + 500 + r, device=self.dev)
+            acc, com, bon = self.model.verify_step(self.ids, tok, q=q, u=u, temperature=temp)
+            rounds.append((tok, q, u))
+            accepted.append(acc.clone())
+            pending = bon.clone()
+        self.model.sync_status()
+        return rounds, torch.stack(accepted).cpu()
+
+    # --------------------------------------------------------- timed replay
+    def replay(self, rounds, warmup, temp, sampler=None):
+        torch = self.torch
+        B, W = self.B, rounds[0][0].shape[1]
+        self.reset()
+        outs = (torch.empty(B, dtype=torch.int32, device=self.dev), torch.empty(B, W, dtype=torch.int32,
+                                                                                device=self.dev),
+                torch.empty(B, dtype=torch.int32, device=self.dev))
+        acc_log = torch.empty(len(rounds), B, dtype=torch.int32, device=self.dev)
+        for r in range(warmup):
+            tok, q, u = rounds[r]
+            self.model.verify_step(self.ids, tok, q=q, u=u, temperature=temp, outs=outs)
+            acc_log[r].copy_(outs[0])
+        launches = self.model.last_launch_count()
+        self._barrier()
+        torch.cuda.synchronize()
+        if sampler:
+            sampler.start()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for r in range(warmup, len(rounds)):
+            tok, q, u = rounds[r]
+            self.model.verify_step(self.ids, tok, q=q, u=u, temperature=temp, outs=outs)
+            acc_log[r].copy_(outs[0])
+        e1.record()
+        torch.cuda.synchronize()
+        clocks = sampler.stop() if sampler else None
+        self._barrier()
+        self.model.sync_status()
+        return e0.elapsed_time(e1), acc_log.cpu(), launches, clocks
+
+    def replay_e2e(self, rounds, warmup, temp):
+        """Same rounds, inputs from pinned host memory and outputs read back every step."""
+        torch = self.torch
+        B, W = self.B, rounds[0][0].shape[1]
+        host = [(t.cpu().pin_memory(), q.cpu().pin_memory(), u.cpu().pin_memory()) for t, q, u in rounds]
+        d_tok = torch.empty_like(rounds[0][0])
+        d_q = torch.empty_like(rounds[0][1])
+        d_u = torch.empty_like(rounds[0][2])
+        outs = (torch.empty(B, dtype=torch.int32, device=self.dev), torch.empty(B, W, dtype=torch.int32,
+                                                                                device=self.dev),
+                torch.empty(B, dtype=torch.int32, device=self.dev))
+        h_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+        acc_log = []
+
+        def step(r):
+            t, q, u = host[r]
+            d_tok.copy_(t, non_blocking=True)
+            d_q.copy_(q, non_blocking=True)
+            d_u.copy_(u, non_blocking=True)
+            self.model.verify_step(self.ids, d_tok, q=d_q, u=d_u, temperature=temp, outs=outs)
+            for h, o in zip(h_out, outs):
+                h.copy_(o, non_blocking=True)
+
+        self.reset()
+        for r in range(warmup):
+            step(r)
+        torch.cuda.synchronize()
+        self._barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for r in range(warmup, len(rounds)):
+            step(r)
+            torch.cuda.current_stream().synchronize()   # the host reads this step's result
+            acc_log.append(h_out[0].clone())
+        e1.record()
+        torch.cuda.synchronize()
+        self._barrier()
+        h2d = sum(x.numel() * x.element_size() for x in host[0])
+        d2h = sum(o.numel() * o.element_size() for o in outs)
+        return e0.elapsed_time(e1), torch.stack(acc_log), h2d, d2h
+
+    def profile(self, rounds, warmup, temp, n):
+        self.reset()
+        outs = None
+        for r in range(warmup):
+            tok, q, u = rounds[r]
+            outs = self.model.verify_step(self.ids, tok, q=q, u=u, temperature=temp, outs=outs)
+        self.model.read_profile()
+        self.model.set_profiling(True)
+        agg = {}
+        for r in range(warmup, min(len(rounds), warmup + n)):
+            tok, q, u = rounds[r]
+            outs = self.model.verify_step(self.ids, tok, q=q, u=u, temperature=temp, outs=outs)
+            for k, (ms, cnt, by) in self.model.read_profile().items():
+                a = agg.setdefault(k, [0.0, 0, 0.0])
+                a[0] += ms
+                a[1] += cnt
+                a[2] += by
+        self.model.set_profiling(False)
+        return agg
+
+    def width_sweep(self, widths, steps, warmup):
+        """T_verify(W) / T_decode at the same batch and context: sampled rounds whose
+        drafts are rejected (q one-hot on a random token), so the context stays ~ctx."""
+        torch = self.torch
+        B, V = self.B, self.dims.vocab
+        res = {}
+        t_dec = None
+        g = torch.Generator(device=self.dev)
+        g.manual_seed(7)
+        for W in widths:
+            pending = self.reset()
+            if W == 1:
+                u = torch.full((B,), 0.5, device=self.dev)
+                nxt = torch.empty(B, dtype=torch.int32, device=self.dev)
+                run = lambda: self.model.decode_step(self.ids, pending, temperature=1.0, u=u, out=nxt)
+            else:
+                tok = torch.randint(0, V, (B, W), generator=g, device=self.dev, dtype=torch.int64).int()
+                tok[:, 0] = pending
+                q = torch.zeros(B, W - 1, V, device=self.dev)
+                q.scatter_(2, tok[:, 1:].long().unsqueeze(-1), 1.0)
+                u = torch.full((B, W), 0.5, device=self.dev)
+                outs = (torch.empty(B, dtype=torch.int32, device=self.dev),
+                        torch.empty(B, W, dtype=torch.int32, device=self.dev),
+                        torch.empty(B, dtype=torch.int32, device=self.dev))
+                run = lambda: self.model.verify_step(self.ids, tok, q=q, u=u, temperature=1.0, outs=outs)
+            for _ in range(warmup):
+                run()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(steps):
+                run()
+            e1.record()
+            torch.cuda.synchronize()
+            self.model.sync_status()
+            ms = e0.elapsed_time(e1) / steps
+            if W == 1:
+                t_dec = ms
+            res[W] = ms
+        return {str(W): {"ms": round(ms, 4), "ratio_to_decode": round(ms / t_dec, 4)} for W, ms in res.items()}
+
+    def _barrier(self):
+        torch = self.torch
+        if torch.distributed.is_available() and torch.distributed.is_initialized():
+            torch.distributed.barrier()
+
+
+def weight_bytes(dims):
+    d, F, V, L = dims.d_model, dims.ffn_dim, dims.vocab, dims.n_layers
+    per_layer = (dims.q_dim + 2 * dims.kv_dim) * d + d * dims.q_dim + 2 * F * d + d * F
+    return 2.0 * (L * per_layer + V * d)
+
+
+# ---------------------------------------------------------- CPU oracle timing
+class OracleSample:
+    """The oracle on a bounded sample of the workload: verify rounds of width gamma+1
+    over `cpu_layers` decoder layers + the LM head at the 8B shape, B = 1, with a
+    cache of `ctx` tokens of N(0,1)*0.5 values (attention time does not depend on
+    them).  Drafts come from q = (1-lam) p + lam Dir(1) with p the oracle's own
+    target at the draft prefix (untimed, like the GPU arm's drafts).  A round's
+    per-layer time is scaled to 32 layers."""
+
+    def __init__(self, args):
+        import numpy as np
+        import torch
+
+        from oracle.decoder import OracleDecoder, weights_to_numpy
+        from speculative_decoding_verify_step_gb300 import synth
+        self.np, self.args = np, args
+        self.dims = synth.LLAMA8B.with_layers(args.cpu_layers)
+        self.W = args.gamma + 1
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        w = weights_to_numpy({k: v.cpu() for k, v in synth.iter_weights(self.dims, seed=11, device=dev)})
+        room = args.ctx + 64 * 8
+        self.o = OracleDecoder(self.dims, w, max_batch=1, max_seq_len=room, num_pages=room // 64 + 2)
+        self.o.kv.ensure(0, args.ctx)
+        rng = np.random.default_rng(3)
+        for pg in self.o.kv.table[0]:
+            self.o.kv.k[:, pg] = rng.normal(size=self.o.kv.k[:, pg].shape) * 0.5
+            self.o.kv.v[:, pg] = rng.normal(size=self.o.kv.v[:, pg].shape) * 0.5
+        self.o.kv.length[0] = args.ctx
+        self.rng = rng
+        self.pending = int(rng.integers(0, self.dims.vocab))
+        self.o.forward([0], np.array([[self.pending]]))    # widen the weights to float64 once (cached)
+        self.r = 0
+
+    def step(self):
+        """One round; returns (scaled seconds, committed tokens, raw sample seconds)."""
+        import time as _t
+
+        from oracle import accept as A
+        from speculative_decoding_verify_step_gb300 import synth
+        np, a, o, W, V = self.np, self.args, self.o, self.W, self.dims.vocab
+        g = W - 1
+        tok = np.zeros((1, W), np.int64)
+        tok[0, 0] = self.pending
+        q = np.zeros((1, g, V), np.float32)
+        D = synth.dirichlet1((1, g, V), seed=900 + self.r).numpy()
+        for i in range(1, W):
+            p = A.target_probs(o.forward([0], tok[:, :i])[:, i - 1], a.temperature).astype(np.float64)
+            qi = (1 - a.lam) * p + a.lam * D[:, i - 1]
+            q[:, i - 1] = qi.astype(np.float32)
+            c = np.cumsum(qi[0])
+            tok[0, i] = min(int(np.searchsorted(c, self.rng.random() * c[-1], side="right")), V - 1)
+        u = synth.uniforms((1, W), seed=950 + self.r).numpy()
+        t0 = _t.perf_counter()
+        logits, hid = o.forward([0], tok, return_hidden=True)
+        p = A.target_probs(logits, a.temperature)
+        n, com, bonus, _ = A.accept_stochastic(p, q, tok[:, 1:], u)
+        t1 = _t.perf_counter()
+        _ = hid @ o.w("lm_head").T
+        t2 = _t.perf_counter()
+        o.commit([0], n, W)
+        self.pending = int(bonus[0])
+        self.r += 1
+        head = t2 - t1
+        full = max(t1 - t0 - head, 0.0) / a.cpu_layers * 32 + head
+        return full, int(n[0]) + 1, t1 - t0
+
+    def describe(self):
+        a = self.args
+        return (f"verify rounds of width {self.W} at B=1 over {a.cpu_layers} decoder layers of the 8B shape "
+                f"+ LM head + acceptance, {a.ctx} cached tokens of synthetic KV, drafts from the oracle's own p "
+                f"(lam={a.lam}); per-layer time x 32 layers")
+
+
+def cpu_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = max((i.get("num_threads", 0) for i in threadpool_info()), default=0)
+        if n:
+            return n
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+def run_reference(args):
+    """The oracle as it stands on the host cores: W untimed + K timed sample rounds."""
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    smp = OracleSample(args)
+    for _ in range(min(args.warmup, 1)):
+        smp.step()
+    secs, toks = 0.0, 0
+    for _ in range(args.steps):
+        full, tk, _ = smp.step()
+        secs += full
+        toks += tk
+    value = args.batch * toks / secs
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1000 * secs / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"llama3.1-8b-shape sampled verify round, B={args.batch}/GPU, ctx={args.ctx}, "
+                                   f"gamma={args.gamma} (width {args.gamma + 1}), lam={args.lam}, "
+                                   f"T={args.temperature}"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+                             "sample": smp.describe()},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    import torch
+    rank, local_rank, world = dist_env()
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    hbm_peak, _, peak_src = measured_peaks()
+    b = Bench(args, dev)
+    gamma, lam, temp = args.gamma, args.lam, args.temperature
+    R = args.warmup + args.steps
+    rounds, acc_rec = b.record(R, gamma, lam, temp, seed=17)
+    sampler = ClockSampler(local_rank)
+    ms, acc_rep, launches, clocks = b.replay(rounds, args.warmup, temp, sampler)
+    replay_ok = bool(torch.equal(acc_rep, acc_rec))
+    tokens = float((acc_rep[args.warmup:].double() + 1).sum())
+    # whole job: tokens of all ranks over the slowest rank's time
+    t = torch.tensor([ms, tokens], dtype=torch.float64, device=dev)
+    if world > 1:
+        mx = t.clone()
+        torch.distributed.all_reduce(mx, op=torch.distributed.ReduceOp.MAX)
+        sm = t.clone()
+        torch.distributed.all_reduce(sm, op=torch.distributed.ReduceOp.SUM)
+        ms, tokens = float(mx[0]), float(sm[1])
+    value = tokens / (ms / 1000.0)
+    ms_per_step = ms / args.steps
+    mean_tpr = float((acc_rep[args.warmup:].double() + 1).mean())
+    strict = float(acc_rep[args.warmup:].double().mean()) / gamma if gamma else 0.0
+
+    out = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+           "data": "synthetic: random-init N(0,0.02) bf16 weights, random-token prompts, drafts from "
+                   "q=(1-lam)p+lam*Dir(1) with p the target at the draft prefix",
+           "config": {"workload": f"llama3.1-8b-shape ({args.layers} layers) sampled verify round, "
+                                  f"B={args.batch}/GPU, ctx={args.ctx}, gamma={gamma} (width {gamma + 1}), "
+                                  f"lam={lam}, T={temp}",
+                      "global_batch": args.batch * world, "seq_len": args.ctx, "gamma": gamma, "lam": lam,
+                      "l2": "no flush: every step streams 15 GB of weights (inputs larger than L2)",
+                      "parallelism": f"replicas x{world}"},
+           "gpu_launches": launches * args.steps, "replay_matches_record": replay_ok,
+           "accept": {"tokens_per_round": round(mean_tpr, 4), "strict_accept_rate": round(strict, 4),
+                      "accept_length": round(mean_tpr, 4), "width_proxy": round(mean_tpr / (gamma + 1), 4)},
+           "clocks": clocks}
+
+    if not args.quick:
+        # --- per-kernel roofline (separate profiling pass, events on the launch stream)
+        prof = b.profile(rounds, args.warmup, temp, n=min(args.steps, 20))
+        gemm_cls = ["qkv", "o", "gate_up", "down", "lm_head"]
+        g_ms = sum(prof[c][0] for c in gemm_cls)
+        g_n = sum(prof[c][1] for c in gemm_cls)
+        g_by = sum(prof[c][2] for c in gemm_cls)
+        achieved = g_by / (g_ms / 1000.0) / 1e9 if g_ms > 0 else 0.0
+        per_class = {c: {"launches": prof[c][1], "avg_us": round(1000 * prof[c][0] / max(1, prof[c][1]), 2),
+                         "GBps": round(prof[c][2] / (prof[c][0] / 1000) / 1e9, 1) if prof[c][0] else None}
+                     for c in prof}
+        kv_bytes_alg = 4.0 * b.dims.n_kv_heads * b.dims.head_dim * (args.ctx + gamma + 1) * args.batch
+        if prof["attention"][0] > 0:
+            per_class["attention"]["GBps_algorithmic"] = round(
+                kv_bytes_alg * prof["attention"][1] / (prof["attention"][0] / 1000) / 1e9, 1)
+        out["roofline"] = {"bound": "hbm", "kernel": "gemm_swapab_kernel (all weight-streaming projections)",
+                           "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                           "frac": round(achieved / hbm_peak, 4), "peak_source": f"{peak_src} hbm_gbs",
+                           "bytes_per_launch": round(g_by / max(1, g_n)),
+                           "traffic": None, "per_class": per_class}
+        wb = weight_bytes(b.dims)
+        kvb = kv_bytes_alg * b.dims.n_layers
+        out["step_roofline"] = {"algorithmic_bytes": wb + kvb, "achieved_GBps": round((wb + kvb) / (ms_per_step / 1000)
+                                                                                  / 1e9, 1),
+                                "frac_of_peak": round((wb + kvb) / (ms_per_step / 1000) / 1e9 / hbm_peak, 4),
+                                "ideal_ms_at_peak": round((wb + kvb) / (hbm_peak * 1e9) * 1000, 4)}
+        if not args.no_e2e:
+            e_ms, e_acc, h2d, d2h = b.replay_e2e(rounds, args.warmup, temp)
+            e_tokens = float((e_acc.double() + 1).sum())
+            if world > 1:
+                t = torch.tensor([e_ms, e_tokens], dtype=torch.float64, device=dev)
+                mx = t.clone()
+                torch.distributed.all_reduce(mx, op=torch.distributed.ReduceOp.MAX)
+                sm = t.clone()
+                torch.distributed.all_reduce(sm, op=torch.distributed.ReduceOp.SUM)
+                e_ms, e_tokens = float(mx[0]), float(sm[1])
+            out["e2e"] = {"value": round(e_tokens / (e_ms / 1000), 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                          "d2h_bytes_per_step": d2h, "ms_per_step": round(e_ms / args.steps, 5)}
+        if not args.no_sweep:
+            sw_steps = max(10, min(args.steps, 50))
+            out["t_verify_over_t_decode"] = b.width_sweep(range(1, 9), sw_steps, 3)
+        if not args.no_lam_sweep:
+            lam_res = {}
+            for lm in (0.2, 0.5, 0.8):
+                _, acc = b.record(24, gamma, lm, temp, seed=31 + int(lm * 10))
+                tpr = float((acc.double() + 1).mean())
+                lam_res[str(lm)] = {"tokens_per_round": round(tpr, 4),
+                                    "strict_accept_rate": round(float(acc.double().mean()) / gamma, 4),
+                                    "accepted_tok_s_at_headline_step_time": round(args.batch * tpr / (ms_per_step
+                                                                                                     / 1000), 2)}
+            out["lam_sweep"] = lam_res
+        if rank == 0 and not args.no_cpu_baseline:
+            t_start = time.perf_counter()
+            smp = OracleSample(args)
+            smp.step()
+            secs, toks, raw, n = 0.0, 0, 0.0, 0
+            while n < 3 or (time.perf_counter() - t_start < 20 and n < 10):
+                full, tk, r = smp.step()
+                secs += full
+                toks += tk
+                raw += r
+                n += 1
+            out["cpu_baseline"] = {"value": round(toks / secs, 5), "unit": UNIT, "cores": cpu_threads(),
+                                   "kind": "oracle",
+                                   "sample": smp.describe() + f"; {n} rounds, {raw / n:.2f} s measured per "
+                                             f"sample round, {secs / n:.2f} s scaled"}
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    b.model.close()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,216 @@
+/*
+ * spec_verify.h -- C ABI of the GB300 speculative-decoding verify round.
+ *
+ * One verify round, as the speculative-decoding pages describe it:
+ *   - the target decoder scores W = gamma + 1 rows per sequence in ONE forward
+ *     pass: row 0 is the pending token (the last committed token, whose KV is
+ *     not cached yet), rows 1..gamma are the drafts
+ *     (Lecture 6 "Optimizing Autoregressive Decode", sections 6.1-6.2;
+ *      "Per-step cost versus accepted tokens", "What SGLang actually runs":
+ *      column 0 of the verify block holds the previous bonus token);
+ *   - acceptance: greedy longest matching prefix (temperature 0), or chain
+ *     rejection sampling -- accept x_i while u_i * q_i(x_i) < p_i(x_i), then
+ *     one draw from norm(max(0, p - q)) after a rejection, or the bonus token
+ *     from p_{gamma+1} after full acceptance (Lecture 6, sections 6.2, 7.1,
+ *     7.4; Leviathan Algorithm 1);
+ *   - commit: the KV cache keeps the committed sequence minus its last token;
+ *     after accepting n drafts the cached length becomes L + 1 + n and pages
+ *     wholly beyond it return to the pool (Lecture 6, sections 6.2 and 11:
+ *     rollback is a length edit of the block table).  Pages hold 64 tokens
+ *     (the ninfer draft-depth sweep, "kPagedKVPageSize = 64").
+ *
+ * Conventions for every entry point
+ *   - Tensor arguments are DEVICE pointers owned by the caller unless the
+ *     comment says "host".  Row-major, no padding, int32 token ids, fp32
+ *     probabilities/uniforms/logits.
+ *   - All work is enqueued on `stream` (a cudaStream_t, NULL = legacy default
+ *     stream) and is asynchronous; outputs are valid once the stream has
+ *     synchronised.  Steps never allocate device memory.
+ *   - Status return only.  Argument errors are detected on the host before any
+ *     launch and return SPEC_ERR_INVALID_ARG with nothing enqueued.  Errors only
+ *     the device can see (a token id out of range, an exhausted page pool, a
+ *     bounded wait that ran out) set a device status word: the call that
+ *     enqueued the work still returns SPEC_OK, and the next spec_sync_status()
+ *     returns the code (and clears it).  Kernels that hit such an error skip the
+ *     offending memory accesses, so the context stays usable.
+ *   - A sampled (temperature > 0) round with q or u missing is an error; the
+ *     library never falls back to greedy.
+ *   - spec_last_error() gives a thread-local message for the last failure.
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum spec_status {
+  SPEC_OK = 0,
+  SPEC_ERR_INVALID_ARG = 1,
+  SPEC_ERR_UNSUPPORTED_DEVICE = 2, /* not an sm_103 GPU */
+  SPEC_ERR_OOM = 3,                /* cudaMalloc failed at create */
+  SPEC_ERR_CAPACITY = 4,           /* no free KV page / sequence longer than max_seq_len */
+  SPEC_ERR_CUDA = 5,               /* a CUDA runtime call failed */
+  SPEC_ERR_TIMEOUT = 6,            /* a bounded device-side wait ran out */
+  SPEC_ERR_UNSUPPORTED = 7         /* a shape the kernels do not handle */
+} spec_status;
+
+/* Decoder shape and pool sizes.  d_model, n_heads*head_dim, n_kv_heads*head_dim
+ * and ffn_dim must be multiples of 128 and vocab a multiple of 128; head_dim is
+ * 64 or 128; n_heads a multiple of n_kv_heads with n_heads/n_kv_heads <= 8. */
+typedef struct spec_config {
+  int32_t n_layers, d_model, n_heads, n_kv_heads, head_dim, ffn_dim, vocab;
+  float rms_eps;     /* RMSNorm epsilon inside the root */
+  float rope_theta;  /* RoPE base; half-split pairs (i, i + head_dim/2) */
+  int32_t page_size; /* tokens per KV page; must be 64 */
+  int32_t max_batch; /* sequence slots; sequence ids are 0..max_batch-1 */
+  int32_t max_width; /* rows per sequence in one forward (gamma + 1 or tree nodes), 1..16 */
+  int32_t max_seq_len; /* cached tokens per sequence, <= 65536 */
+  int32_t num_pages; /* KV page pool size (pages of page_size tokens, all layers) */
+} spec_config;
+
+/* Weight tensors (standard Llama layout, row-major [out, in]).
+ * Matrices are bf16, norm gains fp32.  `layer` is ignored for the global ones. */
+typedef enum spec_weight {
+  SPEC_W_EMBED = 0,      /* [vocab, d_model] bf16 */
+  SPEC_W_LM_HEAD = 1,    /* [vocab, d_model] bf16 (untied) */
+  SPEC_W_FINAL_NORM = 2, /* [d_model] fp32 */
+  SPEC_W_ATTN_NORM = 3,  /* [d_model] fp32 */
+  SPEC_W_WQ = 4,         /* [n_heads*head_dim, d_model] bf16 */
+  SPEC_W_WK = 5,         /* [n_kv_heads*head_dim, d_model] bf16 */
+  SPEC_W_WV = 6,         /* [n_kv_heads*head_dim, d_model] bf16 */
+  SPEC_W_WO = 7,         /* [d_model, n_heads*head_dim] bf16 */
+  SPEC_W_FFN_NORM = 8,   /* [d_model] fp32 */
+  SPEC_W_GATE = 9,       /* [ffn_dim, d_model] bf16 */
+  SPEC_W_UP = 10,        /* [ffn_dim, d_model] bf16 */
+  SPEC_W_DOWN = 11       /* [d_model, ffn_dim] bf16 */
+} spec_weight;
+
+typedef struct spec_model spec_model; /* opaque; owned by the library */
+
+/* Create a model on the current CUDA device: validates cfg, allocates the weight
+ * arena, the KV page pool, the sequence state and every workspace, all at once.
+ * Weights start as zeros; load them with spec_model_set_weight.  All sequences
+ * start empty.  Returns SPEC_ERR_UNSUPPORTED_DEVICE on anything but sm_103. */
+spec_status spec_model_create(const spec_config* cfg, spec_model** out);
+
+/* Free everything the model owns.  Synchronises the device first.  NULL is a no-op. */
+void spec_model_destroy(spec_model* m);
+
+/* Copy one weight tensor into the model (the library repacks it into its own
+ * layout).  src may be a device or a host pointer (cudaMemcpyDefault);
+ * n_elems must equal the tensor's size.  Enqueued on `stream`. */
+spec_status spec_model_set_weight(spec_model* m, spec_weight which, int32_t layer,
+                                  const void* src, int64_t n_elems, void* stream);
+
+/* Empty the given sequences (host ids) and return their pages to the pool. */
+spec_status spec_seq_reset(spec_model* m, int32_t n, const int32_t* seq_ids_host, void* stream);
+
+/* Prefill: append prompt[:-1] of each sequence to its cache; the last prompt
+ * token becomes the pending token, which the caller passes as row 0 of the next
+ * decode/verify call.  tokens: device [B, stride] (row b holds lens_host[b]
+ * tokens); seq_ids: device [B]; lens_host: HOST [B], each >= 1.  Runs the
+ * target forward in windows of max_width rows per sequence. */
+spec_status spec_prefill(spec_model* m, int32_t B, const int32_t* seq_ids, const int32_t* tokens,
+                         int32_t stride, const int32_t* lens_host, void* stream);
+
+/* Baseline decode step (q_len = 1): one forward over the pending tokens tok[B],
+ * then argmax (temperature == 0) or one draw from softmax(logits/T) with u[B]
+ * (temperature > 0; u required).  Writes next_tok[B] and commits (L += 1). */
+spec_status spec_decode_step(spec_model* m, int32_t B, const int32_t* seq_ids, const int32_t* tok,
+                             float temperature, const float* u, int32_t* next_tok, void* stream);
+
+/* Verify round.  tok [B, gamma+1]: pending token + gamma drafts.
+ * temperature == 0: greedy, q and u must be NULL or are ignored.
+ * temperature > 0: q [B, gamma, vocab] fp32 draft distributions (q[b, i-1] is
+ * the distribution draft x_i was drawn from, over the same temperature-adjusted
+ * vocabulary), u [B, gamma+1] fp32 uniforms in [0,1): u[b, i-1] drives the test
+ * of x_i and u[b, gamma] the one final draw.
+ * Outputs: accepted [B] = n_b; committed [B, gamma+1] = x_1..x_n then the
+ * resampled or bonus token, -1 after; bonus [B] = that last token.
+ * Commits L <- L + 1 + n_b and frees trailing pages.  1 <= gamma+1 <= max_width. */
+spec_status spec_verify_step(spec_model* m, int32_t B, int32_t gamma, const int32_t* seq_ids,
+                             const int32_t* tok, const float* q, const float* u, float temperature,
+                             int32_t* accepted, int32_t* committed, int32_t* bonus, void* stream);
+
+/* Greedy token-tree verify (Lecture 6 section 10.3).  tok [B, n_nodes], node 0 =
+ * pending token; parent_host: HOST [n_nodes], parent[0] = -1 and
+ * 0 <= parent[c] < c (BFS order).  One forward under the ancestor mask (node c
+ * at position L + depth(c), KV slot L + c); the accepted path is the longest
+ * root-to-node walk whose tokens equal the target argmax at their parent
+ * (lowest node index among equal siblings).  Outputs: accepted [B] = path
+ * length n; committed [B, n_nodes]: path tokens then the bonus token, -1 after;
+ * bonus [B].  The path's KV (all layers) is moved to slots L+1..L+n, then the
+ * cache is cut to L + 1 + n.  n_nodes <= max_width. */
+spec_status spec_verify_tree_step(spec_model* m, int32_t B, int32_t n_nodes, const int32_t* seq_ids,
+                                  const int32_t* tok, const int32_t* parent_host,
+                                  int32_t* accepted, int32_t* committed, int32_t* bonus, void* stream);
+
+/* Forward only: score W rows per sequence (chain, or tree if parent_host != NULL)
+ * and write the window's KV, without changing any committed length.  logits_out
+ * (device [B, W, vocab] fp32) may be NULL. */
+spec_status spec_score(spec_model* m, int32_t B, int32_t W, const int32_t* seq_ids, const int32_t* tok,
+                       const int32_t* parent_host, float* logits_out, void* stream);
+
+/* Standalone acceptance on given probabilities (no model): p [B, gamma+1, V]
+ * fp32 target probabilities (row j = distribution after row j's token),
+ * q [B, gamma, V], x [B, gamma] drafts, u [B, gamma+1].  Same decision code as
+ * spec_verify_step; bit-exact by construction (fp32 products, integer CDF). */
+spec_status spec_accept_probs(int32_t B, int32_t gamma, int32_t V, const float* p, const float* q,
+                              const int32_t* x, const float* u, int32_t* accepted, int32_t* committed,
+                              int32_t* bonus, void* stream);
+
+/* Standalone greedy acceptance on given logits [B, gamma+1, V] and drafts x [B, gamma]. */
+spec_status spec_accept_greedy(int32_t B, int32_t gamma, int32_t V, const float* logits, const int32_t* x,
+                               int32_t* accepted, int32_t* committed, int32_t* bonus, void* stream);
+
+/* Synchronous host copy of the sequence state for tests: seq_len_host [n] and
+ * page_table_host [n, max_pages_per_seq] (-1 = no page). */
+spec_status spec_get_kv_state(spec_model* m, int32_t n, const int32_t* seq_ids_host, int32_t* seq_len_host,
+                              int32_t* page_table_host);
+
+/* Synchronous host copy of cached K and V (bf16 bits) of one sequence, slots
+ * [t0, t0+n), layer `layer`: k_host and v_host are [n, n_kv_heads, head_dim] uint16. */
+spec_status spec_read_kv(spec_model* m, int32_t layer, int32_t seq_id, int32_t t0, int32_t n,
+                         uint16_t* k_host, uint16_t* v_host);
+
+/* Copy the last forward's logits ([rows, vocab] fp32, rows = B*W of that call)
+ * to `out` (device or host).  Enqueued on `stream`. */
+spec_status spec_debug_logits(spec_model* m, float* out, int64_t max_elems, void* stream);
+
+/* Timing aid for long contexts: give each sequence (host ids) lens_host[b]
+ * cached tokens with pseudo-random bf16 K/V (a hash of seed and position, scaled
+ * by `scale`), without running the model.  Attention time does not depend on
+ * the values. */
+spec_status spec_kv_fill_random(spec_model* m, int32_t n, const int32_t* seq_ids_host, const int32_t* lens_host,
+                                uint64_t seed, float scale, void* stream);
+
+/* Per-kernel timing for reports.  While enabled, every weight-streaming
+ * projection launch and every attention launch of a forward is bracketed by CUDA
+ * events on the call's stream (this serialises those launches; use it in a
+ * separate measuring pass).  Classes: 0 QKV, 1 O, 2 gate/up, 3 down, 4 LM head,
+ * 5 attention (+ merge).  spec_read_profile synchronises the device, adds the
+ * recorded durations to ms[6] and launch counts to launches[6], and its
+ * algorithmic HBM bytes (weights; K/V pages read) to bytes[6], then clears the
+ * record.  At most 1024 launches are recorded between two reads. */
+spec_status spec_set_profiling(spec_model* m, int32_t enable);
+spec_status spec_read_profile(spec_model* m, double* ms, int64_t* launches, double* bytes);
+
+/* Synchronise `stream`, return and clear the device status word. */
+spec_status spec_sync_status(spec_model* m, void* stream);
+
+/* Pages per sequence in the page table (ceil(max_seq_len / page_size)). */
+int32_t spec_max_pages_per_seq(const spec_model* m);
+
+/* Number of kernel launches the last forward/round enqueued (for reports). */
+int32_t spec_last_launch_count(const spec_model* m);
+
+/* Message for the last error on this thread ("" if none). */
+const char* spec_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPEC_VERIFY_H */

@@ -1,0 +1,335 @@
+// Acceptance of the verify round: logits -> (argmax | softmax statistics) ->
+// accept / resample / bonus -> commit.
+//
+// Greedy ("Per-step cost versus accepted tokens", "What SGLang actually runs";
+// Lecture 6 "Optimizing Autoregressive Decode" section 7.4): compare each draft
+// with the target argmax at its position, accept the longest matching prefix,
+// and commit the target argmax at the first mismatch (or after the last draft).
+//
+// Sampled (Lecture 6 section 6.2, Leviathan Algorithm 1): accept x_i while
+// u_i * q_i(x_i) < p_i(x_i) (fp32 product, no fused multiply-add); after a
+// rejection at position n+1 draw from norm(max(0, p_{n+1} - q_{n+1})); after
+// full acceptance draw the bonus from p_{gamma+1}.  The one final draw is an
+// integer inverse CDF: masses R_v = floor(r_v * 2^40) as 64-bit integers, their
+// exact sum S, target t = floor(floor(u * 2^24) * S / 2^24), answer = smallest v
+// whose running sum exceeds t.  Integer sums do not depend on the reduction
+// order, so the draw is reproducible bit for bit against a sequential CPU
+// computation on the same probabilities.  If the residual has no mass on that
+// grid the draw falls back to p at the same row.
+//
+// Tree (section 10.3): walk from the root to the child whose token equals the
+// argmax at the current node (lowest node index on ties), then move the
+// accepted path's KV into consecutive slots and cut the cache.
+#include <math.h>
+
+#include "kvstate.cuh"
+#include "launch.cuh"
+
+namespace spec {
+
+namespace {
+
+constexpr int kAccThreads = 1024;
+
+struct ArgMax {
+  float v;
+  int i;
+};
+
+SPEC_DEVICE_INLINE ArgMax better(ArgMax a, ArgMax b) {
+  if (b.v > a.v || (b.v == a.v && b.i < a.i)) return b;
+  return a;
+}
+
+SPEC_DEVICE_INLINE ArgMax warp_argmax(ArgMax a) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    ArgMax b;
+    b.v = __shfl_xor_sync(0xffffffffu, a.v, o);
+    b.i = __shfl_xor_sync(0xffffffffu, a.i, o);
+    a = better(a, b);
+  }
+  return a;
+}
+
+// One block per row: argmax (lowest index on ties) and, for sampled rounds, the
+// row max and sum_v exp((l_v - max) / T).
+__global__ void __launch_bounds__(kAccThreads) row_stats_kernel(const float* rows, int V, float inv_temp, int sampled,
+                                                                int32_t* argmax, float* row_max, float* row_sum) {
+  __shared__ ArgMax sa[32];
+  __shared__ float sf[32];
+  pdl_wait();
+  pdl_launch_dependents();
+  const float* r = rows + (long long)blockIdx.x * V;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  ArgMax best{-INFINITY, 0x7fffffff};
+  for (int v = threadIdx.x; v < V; v += kAccThreads) best = better(best, ArgMax{r[v], v});
+  best = warp_argmax(best);
+  if (lane == 0) sa[warp] = best;
+  __syncthreads();
+  if (warp == 0) {
+    ArgMax a = lane < kAccThreads / 32 ? sa[lane] : ArgMax{-INFINITY, 0x7fffffff};
+    a = warp_argmax(a);
+    if (lane == 0) sa[0] = a;
+  }
+  __syncthreads();
+  best = sa[0];
+  if (threadIdx.x == 0) argmax[blockIdx.x] = best.i == 0x7fffffff ? 0 : best.i;
+  if (!sampled) return;
+  const float mx = best.v;
+  float s = 0.f;
+  for (int v = threadIdx.x; v < V; v += kAccThreads) s += expf((r[v] - mx) * inv_temp);
+  s = warp_sum(s);
+  if (lane == 0) sf[warp] = s;
+  __syncthreads();
+  if (warp == 0) {
+    float t = lane < kAccThreads / 32 ? sf[lane] : 0.f;
+    t = warp_sum(t);
+    if (lane == 0) {
+      row_max[blockIdx.x] = mx;
+      row_sum[blockIdx.x] = t;
+    }
+  }
+}
+
+// Exclusive block scan of 64-bit values; returns the prefix, total via *total.
+SPEC_DEVICE_INLINE unsigned long long block_exscan_u64(unsigned long long v, unsigned long long* sh,
+                                                       unsigned long long* total) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  unsigned long long inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += y;
+  }
+  if (lane == 31) sh[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = blockDim.x >> 5;
+    unsigned long long w = lane < nw ? sh[lane] : 0ull;
+    unsigned long long winc = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long y = __shfl_up_sync(0xffffffffu, winc, o);
+      if (lane >= o) winc += y;
+    }
+    if (lane < nw) sh[lane] = winc - w;  // exclusive warp offsets
+    if (lane == nw - 1) sh[32] = winc;
+  }
+  __syncthreads();
+  const unsigned long long pre = sh[warp] + inc - v;
+  *total = sh[32];
+  __syncthreads();
+  return pre;
+}
+
+template <bool SAMPLED, PSource SRC>
+__global__ void __launch_bounds__(kAccThreads) accept_chain_kernel(const __grid_constant__ AcceptParams p) {
+  __shared__ int s_n, s_tok, s_zero;
+  __shared__ unsigned long long s_scan[33];
+  pdl_wait();
+  pdl_launch_dependents();
+  const int b = blockIdx.x;
+  const int W = p.gamma + 1;
+  const int V = p.V;
+  const long long row0 = (long long)b * W;
+
+  auto xdraft = [&](int i) -> int { return p.tok[(long long)b * p.tok_stride + p.tok_offset + i - 1]; };
+  auto prob = [&](int row, int v) -> float {
+    const float* r = p.rows + (row0 + row) * V;
+    if constexpr (SRC == PSource::kProbs) {
+      return r[v];
+    } else {
+      return expf((r[v] - p.row_max[row0 + row]) * p.inv_temp) / p.row_sum[row0 + row];
+    }
+  };
+
+  // Standalone greedy acceptance has no row-statistics pass: take the argmax of
+  // the W rows here (lowest index on ties).
+  __shared__ int s_am[kMaxWidth];
+  __shared__ ArgMax s_red[32];
+  if constexpr (!SAMPLED) {
+    if (p.row_argmax == nullptr) {
+      const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+      for (int row = 0; row < W; ++row) {
+        const float* r = p.rows + (row0 + row) * V;
+        ArgMax best{-INFINITY, 0x7fffffff};
+        for (int v = threadIdx.x; v < V; v += kAccThreads) best = better(best, ArgMax{r[v], v});
+        best = warp_argmax(best);
+        if (lane == 0) s_red[warp] = best;
+        __syncthreads();
+        if (warp == 0) {
+          ArgMax a = lane < kAccThreads / 32 ? s_red[lane] : ArgMax{-INFINITY, 0x7fffffff};
+          a = warp_argmax(a);
+          if (lane == 0) s_am[row] = a.i == 0x7fffffff ? 0 : a.i;
+        }
+        __syncthreads();
+      }
+    }
+  }
+  auto am = [&](int row) -> int { return p.row_argmax ? p.row_argmax[row0 + row] : s_am[row]; };
+
+  if (threadIdx.x == 0) {
+    int n = 0;
+    for (int i = 1; i <= p.gamma; ++i) {
+      const int x = xdraft(i);
+      bool acc;
+      if (x < 0 || x >= V) {
+        set_status(p.status, SPEC_ERR_INVALID_ARG);
+        acc = false;
+      } else if constexpr (SAMPLED) {
+        const float qx = p.q[((long long)b * p.gamma + (i - 1)) * V + x];
+        acc = __fmul_rn(p.u[row0 + i - 1], qx) < prob(i - 1, x);
+      } else {
+        acc = x == am(i - 1);
+      }
+      if (!acc) break;
+      ++n;
+    }
+    s_n = n;
+    s_zero = 0;
+    if constexpr (!SAMPLED) s_tok = am(n);
+  }
+  __syncthreads();
+  const int n = s_n;
+
+  if constexpr (SAMPLED) {
+    const bool rejected = n < p.gamma;
+    const float* qn = rejected ? p.q + ((long long)b * p.gamma + n) * V : nullptr;
+    const int chunk = (V + kAccThreads - 1) / kAccThreads;
+    const int v0 = min(V, threadIdx.x * chunk), v1 = min(V, v0 + chunk);
+    const float uf = p.u[row0 + p.gamma];
+    const unsigned long long m = (unsigned long long)floorf(uf * 16777216.0f);
+    for (int pass = 0; pass < 2; ++pass) {
+      const bool use_resid = rejected && pass == 0;
+      auto mass = [&](int v) -> unsigned long long {
+        const float pv = prob(n, v);
+        const float r = use_resid ? fmaxf(0.f, pv - qn[v]) : pv;
+        return (unsigned long long)floorf(r * 1099511627776.0f);  // r * 2^40, exact
+      };
+      unsigned long long local = 0;
+      for (int v = v0; v < v1; ++v) local += mass(v);
+      unsigned long long S;
+      const unsigned long long pre = block_exscan_u64(local, s_scan, &S);
+      if (S == 0ull) {
+        if (threadIdx.x == 0) s_zero = 1;
+        if (!use_resid) {  // p itself has no mass on the grid: cannot happen for a distribution
+          if (threadIdx.x == 0) s_tok = 0;
+          break;
+        }
+        continue;  // fall back to p at the break row
+      }
+      // t = floor(m * S / 2^24) with a 128-bit product (m < 2^24, S < 2^58)
+      const unsigned long long hi = __umul64hi(m, S), lo = m * S;
+      const unsigned long long t = (hi << 40) | (lo >> 24);
+      if (local > 0 && pre <= t && t < pre + local) {
+        unsigned long long run = pre;
+        for (int v = v0; v < v1; ++v) {
+          run += mass(v);
+          if (run > t) {
+            s_tok = v;
+            break;
+          }
+        }
+      }
+      break;
+    }
+    __syncthreads();
+  }
+  const int tok_final = s_tok;
+  for (int j = threadIdx.x; j < W; j += kAccThreads)
+    p.committed[row0 + j] = j < n ? xdraft(j + 1) : (j == n ? tok_final : -1);
+  if (threadIdx.x == 0) {
+    p.accepted[b] = n;
+    p.bonus[b] = tok_final;
+    if (p.seq_ids) {
+      const int s = p.seq_ids[b];
+      if (s >= 0 && s < p.max_batch)
+        truncate_seq(s, min(p.seq_len[s] + 1 + n, p.max_pages * kPage), p.seq_len, p.seq_npages, p.page_table,
+                     p.max_pages, p.free_bits);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kAccThreads) accept_tree_kernel(const __grid_constant__ TreeParams p) {
+  __shared__ int s_path[kMaxWidth];
+  __shared__ int s_n, s_tok;
+  pdl_wait();
+  pdl_launch_dependents();
+  const int b = blockIdx.x;
+  const int N = p.N;
+  const long long row0 = (long long)b * N;
+  if (threadIdx.x == 0) {
+    int v = 0, k = 0, a = 0;
+    while (true) {
+      a = p.row_argmax[row0 + v];
+      int nxt = -1;
+      for (int c = 1; c < N; ++c) {
+        if (p.parent[c] == v && p.tok[row0 + c] == a) {
+          nxt = c;
+          break;
+        }
+      }
+      if (nxt < 0) break;
+      s_path[k++] = nxt;
+      v = nxt;
+    }
+    s_n = k;
+    s_tok = a;
+  }
+  __syncthreads();
+  const int n = s_n;
+  for (int j = threadIdx.x; j < N; j += kAccThreads)
+    p.committed[row0 + j] = j < n ? p.tok[row0 + s_path[j]] : (j == n ? s_tok : -1);
+  const int s = p.seq_ids[b];
+  if (s < 0 || s >= p.max_batch) return;  // flagged by the prepare kernel
+  const int L = p.seq_len[s];
+  // Move the path's KV (all layers, K and V) from slot L + node to slot L + depth.
+  // Destination slots L+1..L+n never coincide with a later source slot (node >= depth).
+  const int vec_per_head = p.hd / 8;  // 16-byte vectors
+  const long long per_tok = (long long)p.n_layers * p.Hkv * vec_per_head;
+  for (long long e = threadIdx.x; e < per_tok * n; e += kAccThreads) {
+    const int d = (int)(e / per_tok) + 1;
+    const long long r = e % per_tok;
+    const int vec = (int)(r % vec_per_head);
+    const int kvh = (int)((r / vec_per_head) % p.Hkv);
+    const int layer = (int)(r / ((long long)vec_per_head * p.Hkv));
+    const int src_t = L + s_path[d - 1], dst_t = L + d;
+    if (src_t / kPage >= p.max_pages) continue;
+    const int src_pg = p.page_table[(long long)s * p.max_pages + src_t / kPage];
+    const int dst_pg = p.page_table[(long long)s * p.max_pages + dst_t / kPage];
+    if (src_pg < 0 || dst_pg < 0) continue;
+    const long long src = ((((long long)layer * p.num_pages + src_pg) * p.Hkv + kvh) * kPage + src_t % kPage) * p.hd;
+    const long long dst = ((((long long)layer * p.num_pages + dst_pg) * p.Hkv + kvh) * kPage + dst_t % kPage) * p.hd;
+    reinterpret_cast<uint4*>(p.kpool + dst)[vec] = reinterpret_cast<const uint4*>(p.kpool + src)[vec];
+    reinterpret_cast<uint4*>(p.vpool + dst)[vec] = reinterpret_cast<const uint4*>(p.vpool + src)[vec];
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    p.accepted[b] = n;
+    p.bonus[b] = s_tok;
+    truncate_seq(s, min(L + 1 + n, p.max_pages * kPage), p.seq_len, p.seq_npages, p.page_table, p.max_pages,
+                 p.free_bits);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_row_stats(const float* rows, int n_rows, int V, float inv_temp, bool sampled, int32_t* argmax,
+                             float* row_max, float* row_sum, cudaStream_t st) {
+  return launch_k(row_stats_kernel, dim3(n_rows), dim3(kAccThreads), 0, st, rows, V, inv_temp, sampled ? 1 : 0,
+                  argmax, row_max, row_sum);
+}
+
+cudaError_t launch_accept_chain(const AcceptParams& p, bool sampled, PSource src, cudaStream_t st) {
+  dim3 grid(p.B), block(kAccThreads);
+  if (!sampled) return launch_k(accept_chain_kernel<false, PSource::kLogits>, grid, block, 0, st, p);
+  if (src == PSource::kProbs) return launch_k(accept_chain_kernel<true, PSource::kProbs>, grid, block, 0, st, p);
+  return launch_k(accept_chain_kernel<true, PSource::kLogits>, grid, block, 0, st, p);
+}
+
+cudaError_t launch_accept_tree(const TreeParams& p, cudaStream_t st) {
+  return launch_k(accept_tree_kernel, dim3(p.B), dim3(kAccThreads), 0, st, p);
+}
+
+}  // namespace spec

@@ -1,0 +1,201 @@
+// Sequence-state kernels: round preparation (page allocation + row metadata),
+// reset, the prefill commit, and the random KV fill used for long-context timing.
+#include <algorithm>
+
+#include "kvstate.cuh"
+#include "launch.cuh"
+
+namespace spec {
+
+namespace {
+
+// One warp.  Sequences are served in batch order b = 0..B-1 (deterministic page
+// assignment).  For each window row j: position L + depth[j] (RoPE), KV slot L + j.
+__global__ void __launch_bounds__(32) prepare_kernel(const __grid_constant__ PrepareParams p) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int lane = threadIdx.x;
+  for (int b = 0; b < p.B; ++b) {
+    const int s = p.seq_ids[b];
+    const bool sid_ok = s >= 0 && s < p.max_batch;
+    int L = 0;
+    bool ok = sid_ok;
+    if (!sid_ok) {
+      if (lane == 0) set_status(p.status, SPEC_ERR_INVALID_ARG);
+    } else {
+      L = p.seq_len[s];
+      if (L + p.W > p.max_seq_len) {
+        ok = false;
+      } else {
+        ok = warp_ensure_pages(s, L + p.W, p.seq_npages, p.page_table, p.max_pages, p.free_bits, p.num_pages);
+      }
+      if (!ok && lane == 0) set_status(p.status, SPEC_ERR_CAPACITY);
+    }
+    if (lane == 0) p.seq_start[b] = L;
+    for (int j = lane; j < p.W; j += 32) {
+      const int m = b * p.W + j;
+      p.row_pos[m] = min(L + p.depth[j], p.max_seq_len - 1);
+      int slot = -1;
+      if (ok) {
+        const int t = L + j;
+        slot = p.page_table[(long long)s * p.max_pages + t / kPage] * kPage + t % kPage;
+      }
+      p.row_slot[m] = slot;
+      const int tk = p.tok[m];
+      if (tk < 0 || tk >= p.vocab) set_status(p.status, SPEC_ERR_INVALID_ARG);
+    }
+    __syncwarp();
+  }
+}
+
+__global__ void seq_reset_kernel(const int32_t* seq_ids, int n, int32_t* seq_len, int32_t* seq_npages,
+                                 int32_t* page_table, uint32_t* free_bits, int max_pages) {
+  pdl_wait();
+  pdl_launch_dependents();
+  if (threadIdx.x != 0) return;
+  for (int i = 0; i < n; ++i) truncate_seq(seq_ids[i], 0, seq_len, seq_npages, page_table, max_pages, free_bits);
+}
+
+// Prefill windows commit every row: L <- L + W.
+__global__ void commit_all_kernel(const int32_t* seq_ids, int B, int W, int max_batch, int32_t* seq_len) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= B) return;
+  const int s = seq_ids[b];
+  if (s >= 0 && s < max_batch) seq_len[s] += W;
+}
+
+// Pages for each listed sequence, in list order (lowest free page first).
+// relative == 0: the sequence gets exactly lens[i] cached tokens (length set).
+// relative == 1: pages are reserved for lens[i] more tokens after the current
+//                length (a prefill reserves its whole prompt up front, so page
+//                assignment follows the caller's sequence order, not the order
+//                in which prefill windows happen to run).  Length unchanged.
+__global__ void __launch_bounds__(32) alloc_to_len_kernel(const int32_t* seq_ids, const int32_t* lens, int n,
+                                                          int relative, int32_t* seq_len, int32_t* seq_npages,
+                                                          int32_t* page_table, uint32_t* free_bits, int max_pages,
+                                                          int num_pages, int max_batch, int* status) {
+  pdl_wait();
+  pdl_launch_dependents();
+  for (int i = 0; i < n; ++i) {
+    const int s = seq_ids[i];
+    if (s < 0 || s >= max_batch) {
+      if (threadIdx.x == 0) set_status(status, SPEC_ERR_INVALID_ARG);
+      continue;
+    }
+    const int upto = relative ? seq_len[s] + lens[i] : lens[i];
+    const bool ok = warp_ensure_pages(s, upto, seq_npages, page_table, max_pages, free_bits, num_pages);
+    if (threadIdx.x == 0) {
+      if (!ok) set_status(status, SPEC_ERR_CAPACITY);
+      if (!relative) seq_len[s] = ok ? lens[i] : 0;
+    }
+    __syncwarp();
+  }
+}
+
+SPEC_DEVICE_INLINE uint64_t splitmix64(uint64_t x) {
+  x += 0x9E3779B97F4A7C15ull;
+  x = (x ^ (x >> 30)) * 0xBF58476D1CE4E5B9ull;
+  x = (x ^ (x >> 27)) * 0x94D049BB133111EBull;
+  return x ^ (x >> 31);
+}
+
+// Fill K and V of every allocated page of the listed sequences, all layers.
+// grid: (pages, n_layers, n); each block writes one (layer, page) of one sequence.
+__global__ void kv_fill_kernel(__nv_bfloat16* kpool, __nv_bfloat16* vpool, const int32_t* page_table,
+                               const int32_t* seq_npages, int max_pages, const int32_t* seq_ids, int num_pages,
+                               int Hkv, int hd, uint64_t seed, float scale) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int s = seq_ids[blockIdx.z];
+  const int layer = blockIdx.y;
+  const int pi = blockIdx.x;
+  if (pi >= seq_npages[s]) return;
+  const int pg = page_table[(long long)s * max_pages + pi];
+  if (pg < 0) return;
+  const long long per_page = (long long)Hkv * kPage * hd;
+  const long long base = ((long long)layer * num_pages + pg) * per_page;
+  for (long long e = threadIdx.x; e < per_page; e += blockDim.x) {
+    const uint64_t h = splitmix64(seed ^ (uint64_t)(base + e) * 0x2545F4914F6CDD1Dull);
+    const float a = ((float)(uint32_t)(h & 0xffffffu) * (1.0f / 16777216.0f) * 2.f - 1.f) * scale;
+    const float c = ((float)(uint32_t)((h >> 32) & 0xffffffu) * (1.0f / 16777216.0f) * 2.f - 1.f) * scale;
+    kpool[base + e] = __float2bfloat16(a);
+    vpool[base + e] = __float2bfloat16(c);
+  }
+}
+
+__global__ void gather_tokens_kernel(const int32_t* tokens, int stride, const int32_t* perm, int k, int col0, int W,
+                                     int32_t* out, const int32_t* seq_ids, int32_t* ids_out) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int i = blockIdx.x;
+  const int b = perm[i];
+  for (int j = threadIdx.x; j < W; j += blockDim.x) out[i * W + j] = tokens[(long long)b * stride + col0 + j];
+  if (threadIdx.x == 0) ids_out[i] = seq_ids[b];
+}
+
+__global__ void init_state_kernel(int32_t* seq_len, int32_t* seq_npages, int32_t* page_table, uint32_t* free_bits,
+                                  int max_batch, int max_pages, int num_pages) {
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < max_batch) {
+    seq_len[i] = 0;
+    seq_npages[i] = 0;
+  }
+  if (i < (long long)max_batch * max_pages) page_table[i] = -1;
+  const int nwords = (num_pages + 31) / 32;
+  if (i < nwords) {
+    const int lo = (int)i * 32;
+    const int valid = min(32, num_pages - lo);
+    free_bits[i] = valid >= 32 ? 0xffffffffu : ((1u << valid) - 1u);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_gather_tokens(const int32_t* tokens, int stride, const int32_t* perm, int k, int col0, int W,
+                                 int32_t* out, const int32_t* seq_ids, int32_t* ids_out, cudaStream_t st) {
+  return launch_k(gather_tokens_kernel, dim3(k), dim3(32), 0, st, tokens, stride, perm, k, col0, W, out, seq_ids,
+                  ids_out);
+}
+
+cudaError_t launch_init_state(int32_t* seq_len, int32_t* seq_npages, int32_t* page_table, uint32_t* free_bits,
+                              int max_batch, int max_pages, int num_pages, cudaStream_t st) {
+  const long long n = std::max<long long>({(long long)max_batch * max_pages, (long long)max_batch,
+                                           (long long)(num_pages + 31) / 32});
+  init_state_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(seq_len, seq_npages, page_table, free_bits,
+                                                                  max_batch, max_pages, num_pages);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prepare(const PrepareParams& p, cudaStream_t st) {
+  return launch_k(prepare_kernel, dim3(1), dim3(32), 0, st, p);
+}
+
+cudaError_t launch_seq_reset(const ResetParams& p, cudaStream_t st) {
+  return launch_k(seq_reset_kernel, dim3(1), dim3(32), 0, st, p.seq_ids, p.n, p.seq_len, p.seq_npages, p.page_table,
+                  p.free_bits, p.max_pages);
+}
+
+cudaError_t launch_commit_all(const int32_t* seq_ids, int B, int W, int max_batch, int32_t* seq_len,
+                              cudaStream_t st) {
+  return launch_k(commit_all_kernel, dim3((B + 127) / 128), dim3(128), 0, st, seq_ids, B, W, max_batch, seq_len);
+}
+
+cudaError_t launch_alloc_to_len(const int32_t* seq_ids, const int32_t* lens, int n, int relative, int32_t* seq_len,
+                                int32_t* seq_npages, int32_t* page_table, uint32_t* free_bits, int max_pages,
+                                int num_pages, int max_batch, int* status, cudaStream_t st) {
+  return launch_k(alloc_to_len_kernel, dim3(1), dim3(32), 0, st, seq_ids, lens, n, relative, seq_len, seq_npages,
+                  page_table, free_bits, max_pages, num_pages, max_batch, status);
+}
+
+cudaError_t launch_kv_fill_pages(__nv_bfloat16* kpool, __nv_bfloat16* vpool, const int32_t* page_table,
+                                 const int32_t* seq_npages, int max_pages, const int32_t* seq_ids, int n,
+                                 int n_layers, int num_pages, int Hkv, int hd, uint64_t seed, float scale,
+                                 cudaStream_t st) {
+  dim3 grid(max_pages, n_layers, n);
+  return launch_k(kv_fill_kernel, grid, dim3(256), 0, st, kpool, vpool, page_table, seq_npages, max_pages, seq_ids,
+                  num_pages, Hkv, hd, seed, scale);
+}
+
+}  // namespace spec

@@ -1,0 +1,310 @@
+"""GPU verify round vs the oracle on the tiny 2-layer decoder (d 256, 4x64 heads,
+SwiGLU 1024, vocab 1024): forward parity, KV/page tables, greedy and sampled
+rounds, decode steps, the token tree, and error paths."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import accept as A
+from speculative_decoding_verify_step_gb300 import synth
+from tests._gpu import cuda_model, greedy_clear, need_gpu, oracle_for, rel_err, stochastic_margin
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-2          # max-abs error relative to max|ref| (bf16 weights, fp32 accumulation)
+KW = dict(max_batch=4, max_width=16, max_seq_len=512, num_pages=40)
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    need_gpu()
+    w = synth.make_weights(synth.TINY, seed=1, gain_jitter=0.1)
+    m = cuda_model(synth.TINY, w, **KW)
+    yield w, m
+    m.close()
+
+
+def _fresh(w, m, prompts):
+    ids = list(range(len(prompts)))
+    m.seq_reset(ids)
+    L = max(len(p) for p in prompts)
+    tok = torch.zeros(len(prompts), L, dtype=torch.int32)
+    for b, p in enumerate(prompts):
+        tok[b, :len(p)] = torch.as_tensor(p)
+    m.prefill(ids, tok.cuda(), [len(p) for p in prompts])
+    o = oracle_for(synth.TINY, w, **KW)
+    o.prefill(ids, prompts)
+    return ids, o
+
+
+def _prompts(lens, seed):
+    g = np.random.default_rng(seed)
+    return [g.integers(0, synth.TINY.vocab, n) for n in lens]
+
+
+def test_forward_logits_and_kv(tiny):
+    w, m = tiny
+    prompts = _prompts([64, 37], 2)
+    ids, o = _fresh(w, m, prompts)
+    lens, pt = m.kv_state(ids)
+    assert lens == [63, 36]
+    np.testing.assert_array_equal(np.array(pt), o.kv.page_table_array(ids))
+    tok = np.stack([np.concatenate([[p[-1]], d]) for p, d in zip(prompts, _prompts([3, 3], 3))])
+    got = m.score(ids, torch.from_numpy(tok).cuda()).cpu().numpy()
+    ref = o.forward(ids, tok)
+    assert rel_err(got, ref) < TOL
+    # cached KV (bf16) against the oracle's (fp64), all layers, prompt and window slots
+    for layer in range(synth.TINY.n_layers):
+        for b, s in enumerate(ids):
+            n = len(prompts[b]) - 1 + 4
+            k, v = m.read_kv(layer, s, 0, n)
+            kr = np.stack([o.kv.k[layer, o.kv.slot(s, t)[0], :, o.kv.slot(s, t)[1]] for t in range(n)])
+            vr = np.stack([o.kv.v[layer, o.kv.slot(s, t)[0], :, o.kv.slot(s, t)[1]] for t in range(n)])
+            assert rel_err(k.float().numpy(), kr) < TOL
+            assert rel_err(v.float().numpy(), vr) < TOL
+
+
+@pytest.mark.parametrize("W", [1, 2, 5, 8, 16])
+def test_window_widths(tiny, W):
+    w, m = tiny
+    prompts = _prompts([130, 64], 10 + W)      # crosses page boundaries; ragged tail
+    ids, o = _fresh(w, m, prompts)
+    tok = np.stack([np.concatenate([[p[-1]], d]) for p, d in zip(prompts, _prompts([W - 1] * 2, 4))])
+    got = m.score(ids, torch.from_numpy(tok).cuda()).cpu().numpy()
+    ref = o.forward(ids, tok)
+    assert rel_err(got, ref) < TOL
+
+
+def test_greedy_rounds_teacher_forced(tiny):
+    """32 greedy verify rounds (gamma = 3, B = 2) with mixed drafts.  Where every row the
+    decision reads has a top-2 gap > 1e-2 the accepted count and committed tokens are
+    identical; near-ties are counted and the GPU state is re-synchronised to the oracle."""
+    w, m = tiny
+    prompts = _prompts([64, 64], 5)
+    ids, o = _fresh(w, m, prompts)
+    hist = [list(map(int, p)) for p in prompts]
+    rng = np.random.default_rng(6)
+    gamma, compared, near = 3, 0, 0
+    for r in range(32):
+        # drafts: the oracle's own greedy continuation, each draft corrupted w.p. 1/4
+        tok = np.zeros((2, gamma + 1), np.int64)
+        tok[:, 0] = [h[-1] for h in hist]
+        for i in range(1, gamma + 1):
+            nxt = o.forward(ids, tok[:, :i])[:, i - 1].argmax(-1)
+            bad = rng.random(2) < 0.25
+            tok[:, i] = np.where(bad, rng.integers(0, synth.TINY.vocab, 2), nxt)
+        ref = o.forward(ids, tok)
+        n_ref, com_ref, _ = A.accept_greedy(ref, tok[:, 1:])
+        acc, com, bon = m.verify_step(ids, torch.from_numpy(tok).cuda())
+        got_logits = m.debug_logits(2 * (gamma + 1)).cpu().numpy().reshape(ref.shape)
+        assert rel_err(got_logits, ref) < TOL
+        clear = greedy_clear(ref, n_ref)
+        acc, com = acc.cpu().numpy(), com.cpu().numpy()
+        for b in range(2):
+            if clear[b]:
+                compared += 1
+                assert acc[b] == n_ref[b]
+                np.testing.assert_array_equal(com[b], com_ref[b])
+            else:
+                near += 1
+        o.commit(ids, n_ref, gamma + 1)
+        for b in range(2):
+            hist[b].extend(int(t) for t in com_ref[b, :n_ref[b] + 1])
+        if not (clear.all() and (acc == n_ref).all()):
+            ids, o2 = _fresh(w, m, [np.array(h) for h in hist])   # re-sync both sides
+            o = o2
+        else:
+            lens, pt = m.kv_state(ids)
+            assert lens == o.lengths(ids).tolist()
+            np.testing.assert_array_equal(np.array(pt), o.kv.page_table_array(ids))
+    assert compared >= 40, (compared, near)
+
+
+def _draft_mixture(o, ids, pending, gamma, lam, temp, seed):
+    """Drafts x_i ~ q_i = (1-lam) p_i + lam Dir(1), p_i the oracle target at the draft
+    prefix (an untimed autoregressive target pass)."""
+    B = len(ids)
+    V = synth.TINY.vocab
+    rng = np.random.default_rng(seed)
+    D = synth.dirichlet1((B, gamma, V), seed=seed).numpy()
+    tok = np.zeros((B, gamma + 1), np.int64)
+    tok[:, 0] = pending
+    q = np.zeros((B, gamma, V), np.float32)
+    for i in range(gamma):
+        logits = o.forward(ids, tok[:, :i + 1])
+        p = A.target_probs(logits[:, i], temp).astype(np.float64)
+        qi = (1 - lam) * p + lam * D[:, i]
+        q[:, i] = qi.astype(np.float32)
+        for b in range(B):
+            c = np.cumsum(q[b, i].astype(np.float64))
+            tok[b, i + 1] = min(int(np.searchsorted(c, rng.random() * c[-1], side="right")), V - 1)
+    return tok, q
+
+
+@pytest.mark.parametrize("lam,temp", [(0.5, 1.0), (0.2, 0.7)])
+def test_sampled_rounds(tiny, lam, temp):
+    """Sampled verify rounds (gamma = 3): bit-exact accepted counts and committed
+    tokens wherever the oracle's decisions are clear of the 1e-2 margins."""
+    w, m = tiny
+    prompts = _prompts([64, 64], 7)
+    ids, o = _fresh(w, m, prompts)
+    gamma, compared, near = 3, 0, 0
+    pending = np.array([p[-1] for p in prompts])
+    hist = [list(map(int, p)) for p in prompts]
+    for r in range(16):
+        tok, q = _draft_mixture(o, ids, pending, gamma, lam, temp, seed=100 + r)
+        u = synth.uniforms((2, gamma + 1), seed=200 + r).numpy()
+        logits = o.forward(ids, tok)
+        p = A.target_probs(logits, temp)
+        n_ref, com_ref, tok_ref, _ = A.accept_stochastic(p, q, tok[:, 1:], u)
+        acc, com, bon = m.verify_step(ids, torch.from_numpy(tok).cuda(), q=torch.from_numpy(q).cuda(),
+                                      u=torch.from_numpy(u).cuda(), temperature=temp)
+        clear = stochastic_margin(p, q, tok[:, 1:], u, n_ref)
+        acc, com = acc.cpu().numpy(), com.cpu().numpy()
+        for b in range(2):
+            if clear[b]:
+                compared += 1
+                assert acc[b] == n_ref[b]
+                np.testing.assert_array_equal(com[b], com_ref[b])
+            else:
+                near += 1
+        o.commit(ids, n_ref, gamma + 1)
+        for b in range(2):
+            hist[b].extend(int(t) for t in com_ref[b, :n_ref[b] + 1])
+        if not ((acc == n_ref).all() and (com == com_ref).all()):
+            ids, o = _fresh(w, m, [np.array(h) for h in hist])   # re-sync both sides
+        pending = com_ref[np.arange(2), n_ref]
+    assert compared >= 16, (compared, near)
+
+
+def test_decode_steps_match_oracle(tiny):
+    w, m = tiny
+    prompts = _prompts([64, 20], 9)
+    ids, o = _fresh(w, m, prompts)
+    pending = np.array([p[-1] for p in prompts])
+    for step in range(12):
+        ref = o.forward(ids, pending[:, None])
+        nxt = m.decode_step(ids, torch.from_numpy(pending).cuda()).cpu().numpy()
+        got = m.debug_logits(2).cpu().numpy()
+        assert rel_err(got, ref[:, 0]) < TOL
+        want = ref[:, 0].argmax(-1)
+        gap = np.sort(ref[:, 0], -1)
+        clear = gap[:, -1] - gap[:, -2] > 1e-2
+        assert (nxt[clear] == want[clear]).all()
+        o.commit(ids, [0, 0], 1)
+        pending = want
+        if not clear.all():
+            return
+    lens, pt = m.kv_state(ids)
+    assert lens == o.lengths(ids).tolist()
+
+
+def test_sampled_decode_step(tiny):
+    w, m = tiny
+    prompts = _prompts([40, 41], 12)
+    ids, o = _fresh(w, m, prompts)
+    pending = np.array([p[-1] for p in prompts])
+    u = np.array([0.3, 0.9], np.float32)
+    ref = o.forward(ids, pending[:, None])
+    p = A.target_probs(ref, 1.0)
+    n_ref, com_ref, tok_ref, _ = A.accept_stochastic(p, np.zeros((2, 0, synth.TINY.vocab), np.float32),
+                                                     np.zeros((2, 0)), u[:, None])
+    nxt = m.decode_step(ids, torch.from_numpy(pending).cuda(), temperature=1.0, u=torch.from_numpy(u).cuda())
+    clear = stochastic_margin(p, np.zeros((2, 0, synth.TINY.vocab), np.float32), np.zeros((2, 0)), u[:, None],
+                              n_ref)
+    got = nxt.cpu().numpy()
+    assert (got[clear] == tok_ref[clear]).all()
+
+
+TREE15 = [-1, 0, 0, 1, 1, 2, 2, 3, 3, 4, 4, 5, 5, 6, 6]    # binary, three levels below the root
+
+
+def test_tree_verify(tiny):
+    """15-node tree: ancestor-masked logits, the greedy walk, path KV compaction and
+    the page table after rollback of the rejected branches."""
+    w, m = tiny
+    prompts = _prompts([100, 70], 13)
+    ids, o = _fresh(w, m, prompts)
+    N = len(TREE15)
+    rng = np.random.default_rng(14)
+    for r in range(6):
+        tok = np.zeros((2, N), np.int64)
+        tok[:, 0] = [o_hist[-1] for o_hist in prompts] if r == 0 else pend
+        tok[:, 1:] = rng.integers(0, synth.TINY.vocab, (2, N - 1))
+        ref = o.forward(ids, tok, parent=np.array(TREE15))
+        am = ref.argmax(-1)
+        for c in range(1, N):                    # plant matches along some branches
+            if rng.random() < 0.6:
+                tok[:, c] = am[:, TREE15[c]]
+                ref = o.forward(ids, tok, parent=np.array(TREE15))
+                am = ref.argmax(-1)
+        n_ref, path, com_ref, bon_ref = A.accept_tree_greedy(ref, tok, np.array(TREE15))
+        acc, com, bon = m.verify_tree_step(ids, torch.from_numpy(tok).cuda(), TREE15)
+        got = m.debug_logits(2 * N).cpu().numpy().reshape(ref.shape)
+        assert rel_err(got, ref) < TOL
+        gap = np.sort(ref, -1)
+        clear = ((gap[..., -1] - gap[..., -2]) > 1e-2).all(axis=1)
+        assert clear.any()
+        acc, com = acc.cpu().numpy(), com.cpu().numpy()
+        for b in range(2):
+            if clear[b]:
+                assert acc[b] == n_ref[b]
+                np.testing.assert_array_equal(com[b, :n_ref[b] + 1], com_ref[b, :n_ref[b] + 1])
+        if not clear.all():
+            return
+        L0 = o.lengths(ids)
+        o.commit_tree(ids, path)
+        lens, pt = m.kv_state(ids)
+        assert lens == o.lengths(ids).tolist()
+        np.testing.assert_array_equal(np.array(pt), o.kv.page_table_array(ids))
+        for b, s in enumerate(ids):              # compacted path KV, layer 0 and last
+            for layer in (0, synth.TINY.n_layers - 1):
+                k, v = m.read_kv(layer, s, int(L0[b]), int(n_ref[b]) + 1)
+                kr = np.stack([o.kv.k[layer, o.kv.slot(s, t)[0], :, o.kv.slot(s, t)[1]]
+                               for t in range(int(L0[b]), int(L0[b]) + int(n_ref[b]) + 1)])
+                assert rel_err(k.float().numpy(), kr) < TOL
+        pend = com_ref[np.arange(2), n_ref]
+
+
+def test_capacity_error_is_reported(tiny):
+    need_gpu()
+    from speculative_decoding_verify_step_gb300 import spec
+    w, _ = tiny
+    m = cuda_model(synth.TINY, w, max_batch=2, max_width=4, max_seq_len=128, num_pages=3)
+    try:
+        m.seq_reset([0, 1])
+        m.prefill([0], torch.zeros(1, 100, dtype=torch.int32).cuda(), [100])   # 99 cached: 2 pages
+        m.sync_status()
+        m.prefill([1], torch.zeros(1, 80, dtype=torch.int32).cuda(), [80])     # needs 2, 1 left
+        with pytest.raises(spec.SpecError) as e:
+            m.sync_status()
+        assert e.value.status == 4
+        m.sync_status()                          # cleared; the context is still usable
+        m.seq_reset([1])
+        m.prefill([1], torch.zeros(1, 10, dtype=torch.int32).cuda(), [10])
+        m.sync_status()
+    finally:
+        m.close()
+
+
+def test_invalid_arguments(tiny):
+    need_gpu()
+    from speculative_decoding_verify_step_gb300 import spec
+    w, m = tiny
+    tok = torch.zeros(2, 4, dtype=torch.int32).cuda()
+    with pytest.raises(spec.SpecError) as e:       # sampled without q/u: never a greedy fallback
+        m.verify_step([0, 1], tok, temperature=1.0)
+    assert e.value.status == 1
+    with pytest.raises(spec.SpecError):
+        m.verify_step(list(range(5)), torch.zeros(5, 4, dtype=torch.int32).cuda())
+    with pytest.raises(spec.SpecError):
+        m.verify_step([0, 1], torch.zeros(2, 17, dtype=torch.int32).cuda())
+    with pytest.raises(spec.SpecError):
+        m.verify_tree_step([0, 1], tok, [-1, 0, 2, 1])
+    bad = torch.full((2, 4), 5000, dtype=torch.int32).cuda()
+    m.seq_reset([0, 1])
+    m.prefill([0, 1], torch.zeros(2, 8, dtype=torch.int32).cuda(), [8, 8])
+    m.verify_step([0, 1], bad)
+    with pytest.raises(spec.SpecError) as e:
+        m.sync_status()
+    assert e.value.status == 1
