@@ -61,6 +61,8 @@ def parse_args():
     ap.add_argument("--no-lam-sweep", action="store_true")
     ap.add_argument("--cpu-layers", type=int, default=2, help="layers in the oracle's timed sample")
     ap.add_argument("--quick", action="store_true", help="a short run for profilers: timed replay only")
+    ap.add_argument("--ncu", action="store_true",
+                    help="profiler mode: cache filled directly (no prefill), fixed drafts, W + K verify rounds")
     return ap.parse_args()
 
 
@@ -443,10 +445,46 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_ncu_mode(args):
+    """Minimal launch sequence for profilers: model creation, a directly filled cache
+    (4 launches: state init, reset, page allocation, fill), then warmup + steps verify
+    rounds with fixed sampled drafts.  Prints the library's launches per round."""
+    import torch
+
+    from speculative_decoding_verify_step_gb300 import spec, synth
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    dims = synth.LLAMA8B.with_layers(args.layers)
+    B, W, V = args.batch, args.gamma + 1, dims.vocab
+    max_seq = args.ctx + 64 * 8
+    m = spec.SpecModel(dims, max_batch=B, max_width=16, max_seq_len=max_seq,
+                       num_pages=B * (-(-max_seq // 64)) + 8)
+    m.load_weights(synth.iter_weights(dims, seed=1, device=dev))
+    m.kv_fill_random(list(range(B)), [args.ctx] * B, seed=5, scale=0.5)
+    ids = torch.arange(B, dtype=torch.int32, device=dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(3)
+    tok = torch.randint(0, V, (B, W), generator=g, device=dev).int()
+    q = synth.dirichlet1((B, W - 1, V), seed=4, device=dev).float()
+    u = synth.uniforms((B, W), seed=6, device=dev)
+    outs = None
+    torch.cuda.synchronize()
+    for _ in range(args.warmup + args.steps):
+        outs = m.verify_step(ids, tok, q=q, u=u, temperature=args.temperature, outs=outs)
+    torch.cuda.synchronize()
+    m.sync_status()
+    print(json.dumps({"ncu_mode": True, "layers": args.layers, "launches_per_round": m.last_launch_count(),
+                      "rounds": args.warmup + args.steps}), flush=True)
+    m.close()
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.ncu:
+        run_ncu_mode(args)
         return
     import torch
     rank, local_rank, world = dist_env()
