@@ -166,6 +166,24 @@ spec_status spec_accept_probs(int32_t B, int32_t gamma, int32_t V, const float* 
 spec_status spec_accept_greedy(int32_t B, int32_t gamma, int32_t V, const float* logits, const int32_t* x,
                                int32_t* accepted, int32_t* committed, int32_t* bonus, void* stream);
 
+/* Greedy acceptance that allocates nothing.  The pages have no counterpart: this
+ * is for callers that cannot call cudaMalloc -- code running inside another
+ * framework's memory pool or a strict memory budget, or a process that must not
+ * allocate once serving has started.  Same inputs and outputs as
+ * spec_accept_greedy, same results; it takes the argmax of each of the
+ * B*(gamma+1) logits rows in its own block (faster when V is large) and keeps
+ * those argmaxes in a fixed scratch array inside the library's device memory
+ * (4096 rows = 16 KB, held on every GPU that loads the library until the process
+ * exits).  B*(gamma+1) > 4096 returns SPEC_ERR_INVALID_ARG.  The first call on a
+ * device looks up the scratch address (cudaGetSymbolAddress) with that device
+ * current; make that first call before any stream capture.  All calls share the
+ * one scratch array: calls that overlap on the GPU (different streams, no
+ * ordering between them) race and give undefined results.  Each row's entry is
+ * rewritten before it is read, so nothing needs clearing between calls. */
+spec_status spec_accept_greedy_noalloc(int32_t B, int32_t gamma, int32_t V, const float* logits,
+                                       const int32_t* x, int32_t* accepted, int32_t* committed,
+                                       int32_t* bonus, void* stream);
+
 /* Synchronous host copy of the sequence state for tests: seq_len_host [n] and
  * page_table_host [n, max_pages_per_seq] (-1 = no page). */
 spec_status spec_get_kv_state(spec_model* m, int32_t n, const int32_t* seq_ids_host, int32_t* seq_len_host,

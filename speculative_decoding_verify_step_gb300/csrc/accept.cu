@@ -22,6 +22,8 @@
 // accepted path's KV into consecutive slots and cut the cache.
 #include <math.h>
 
+#include <mutex>
+
 #include "kvstate.cuh"
 #include "launch.cuh"
 
@@ -332,4 +334,86 @@ cudaError_t launch_accept_tree(const TreeParams& p, cudaStream_t st) {
   return launch_k(accept_tree_kernel, dim3(p.B), dim3(kAccThreads), 0, st, p);
 }
 
+// ------------------------------------------------- allocation-free greedy accept
+// Scratch of spec_accept_greedy_noalloc: the argmax of every logits row, written
+// by the row-statistics kernel and read by the acceptance kernel.  It lives in
+// this library's own device memory (every GPU that loads the library holds it
+// until the process exits), so the entry point never allocates.
+constexpr int kNoAllocMaxRows = 4096;
+static __device__ __align__(256) int32_t g_noalloc_argmax[kNoAllocMaxRows];
+
+namespace {
+
+// Device address of the scratch array on the current device.  Host code cannot
+// use the array's name as a device pointer, so the address is looked up once per
+// device (with that device current) and cached.
+cudaError_t noalloc_scratch(int32_t** out) {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static int32_t* addr[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_argmax);
+    if (e != cudaSuccess) return e;
+    addr[dev] = static_cast<int32_t*>(p);
+  }
+  *out = addr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+
 }  // namespace spec
+
+extern "C" spec_status spec_accept_greedy_noalloc(int32_t B, int32_t gamma, int32_t V, const float* logits,
+                                                  const int32_t* x, int32_t* accepted, int32_t* committed,
+                                                  int32_t* bonus, void* stream) {
+  using namespace spec;
+  if (B < 1 || gamma < 0 || gamma + 1 > kMaxWidth || V < 1) {
+    record_error("spec_accept_greedy_noalloc: bad shape");
+    return SPEC_ERR_INVALID_ARG;
+  }
+  if ((long long)B * (gamma + 1) > kNoAllocMaxRows) {
+    record_error("spec_accept_greedy_noalloc: B*(gamma+1) exceeds the fixed scratch of 4096 rows");
+    return SPEC_ERR_INVALID_ARG;
+  }
+  if (!logits || (gamma > 0 && !x) || !accepted || !committed || !bonus) {
+    record_error("spec_accept_greedy_noalloc: NULL argument");
+    return SPEC_ERR_INVALID_ARG;
+  }
+  int32_t* scratch = nullptr;
+  cudaError_t e = noalloc_scratch(&scratch);
+  if (e != cudaSuccess) {
+    record_error(cudaGetErrorString(e));
+    return SPEC_ERR_CUDA;
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // every row's argmax is rewritten before it is read, so nothing needs clearing
+  e = launch_row_stats(logits, B * (gamma + 1), V, 1.f, false, scratch, nullptr, nullptr, st);
+  if (e == cudaSuccess) {
+    AcceptParams ap{};
+    ap.B = B;
+    ap.gamma = gamma;
+    ap.V = V;
+    ap.inv_temp = 1.f;
+    ap.rows = logits;
+    ap.tok = x;
+    ap.tok_stride = gamma;
+    ap.tok_offset = 0;
+    ap.row_argmax = scratch;
+    ap.accepted = accepted;
+    ap.committed = committed;
+    ap.bonus = bonus;
+    e = launch_accept_chain(ap, false, PSource::kLogits, st);
+  }
+  if (e != cudaSuccess) {
+    record_error(cudaGetErrorString(e));
+    return SPEC_ERR_CUDA;
+  }
+  return SPEC_OK;
+}

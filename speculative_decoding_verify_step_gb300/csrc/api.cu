@@ -16,6 +16,7 @@
 namespace spec {
 bool g_use_pdl = true;
 int g_launch_count = 0;
+void record_error(const char* msg);
 }  // namespace spec
 
 using namespace spec;
@@ -33,6 +34,12 @@ spec_status fail(spec_status s, const char* fmt, ...) {
   g_err = buf;
   return s;
 }
+
+}  // namespace
+
+void spec::record_error(const char* msg) { g_err = msg; }
+
+namespace {
 
 #define CUDA_TRY(expr)                                                                          \
   do {                                                                                          \

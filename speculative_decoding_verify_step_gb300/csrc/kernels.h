@@ -12,6 +12,9 @@ namespace spec {
 // (weight prefetch) overlaps the tail of the kernel before it.
 extern bool g_use_pdl;
 
+// Message for spec_last_error() (thread-local), for entry points outside api.cu.
+void record_error(const char* msg);
+
 // Y_partial[split][m][n] = sum_{k in split} X[m][k] * W[n][k]
 // tmW: weight map, box {64, 128}; tmX: activation map, box {64, BM}; BM in {8,16,32,64}.
 // splits == 1 writes the final result (out[m*ldo + n]).

@@ -42,7 +42,7 @@ EXPORTS = ["spec_model_create", "spec_model_destroy", "spec_model_set_weight", "
            "spec_decode_step", "spec_verify_step", "spec_verify_tree_step", "spec_score", "spec_accept_probs",
            "spec_accept_greedy", "spec_get_kv_state", "spec_read_kv", "spec_debug_logits", "spec_kv_fill_random",
            "spec_sync_status", "spec_max_pages_per_seq", "spec_last_launch_count", "spec_last_error",
-           "spec_set_profiling", "spec_read_profile"]
+           "spec_set_profiling", "spec_read_profile", "spec_accept_greedy_noalloc"]
 
 PROFILE_CLASSES = ["qkv", "o", "gate_up", "down", "lm_head", "attention"]
 
@@ -80,6 +80,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "spec_last_launch_count": (I32, [P]),
         "spec_last_error": (ctypes.c_char_p, []),
         "spec_set_profiling": (I32, [P, I32]),
+        "spec_accept_greedy_noalloc": (I32, [I32, I32, I32, P, P, P, P, P, P]),
         "spec_read_profile": (I32, [P, P, P, P]),
     }
     for name, (res, args) in sig.items():
@@ -274,6 +275,25 @@ def spec_accept_probs(p: torch.Tensor, q: Optional[torch.Tensor], x: Optional[to
     uu = u.float().contiguous()
     _check(lib.spec_accept_probs(B, W - 1, V, _ptr(pp), _ptr(qq), _ptr(xx), _ptr(uu), _ptr(acc), _ptr(com),
                                  _ptr(bon), _stream()))
+    torch.cuda.current_stream().synchronize()
+    return acc, com, bon
+
+
+def spec_accept_greedy_noalloc(logits: torch.Tensor, x: Optional[torch.Tensor], outs=None):
+    """Greedy acceptance through the entry point that allocates nothing in the
+    library (its scratch is a fixed device array, 4096 rows at most).  `outs`
+    lets the caller pass preallocated (accepted, committed, bonus) tensors."""
+    lib = load_library()
+    B, W, V = logits.shape
+    dev = logits.device
+    if outs is None:
+        outs = (torch.empty(B, dtype=torch.int32, device=dev), torch.empty(B, W, dtype=torch.int32, device=dev),
+                torch.empty(B, dtype=torch.int32, device=dev))
+    acc, com, bon = outs
+    xx = None if x is None else _dev_i32(x, dev)
+    lg = logits.float().contiguous()
+    _check(lib.spec_accept_greedy_noalloc(B, W - 1, V, _ptr(lg), _ptr(xx), _ptr(acc), _ptr(com), _ptr(bon),
+                                          _stream()))
     torch.cuda.current_stream().synchronize()
     return acc, com, bon
 
