@@ -20,12 +20,15 @@
 // Tree (section 10.3): walk from the root to the child whose token equals the
 // argmax at the current node (lowest node index on ties), then move the
 // accepted path's KV into consecutive slots and cut the cache.
+#include <cooperative_groups.h>
 #include <math.h>
 
 #include <mutex>
 
 #include "kvstate.cuh"
 #include "launch.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace spec {
 
@@ -253,6 +256,169 @@ __global__ void __launch_bounds__(kAccThreads) accept_chain_kernel(const __grid_
   }
 }
 
+// Merge the LM head's per-128-column statistics of window row `row`: row max,
+// lowest index attaining it, and Z = sum_v exp((l_v - max) / T).  One warp per row;
+// fixed loop and shuffle order, so Z is reproducible.
+SPEC_DEVICE_INLINE void merge_row_stats(const RoundAcceptParams& p, long long m, bool sampled, float* out_max,
+                                        float* out_z, int* out_arg) {
+  const int lane = threadIdx.x & 31;
+  float mx = -INFINITY;
+  int am = 0x7fffffff;
+  for (int t = lane; t < p.n_tiles; t += 32) {
+    const float v = p.tstat_max[(long long)t * p.tstat_stride + m];
+    const int a = p.tstat_arg[(long long)t * p.tstat_stride + m];
+    if (v > mx || (v == mx && a < am)) {
+      mx = v;
+      am = a;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float om = __shfl_xor_sync(0xffffffffu, mx, o);
+    const int oa = __shfl_xor_sync(0xffffffffu, am, o);
+    if (om > mx || (om == mx && oa < am)) {
+      mx = om;
+      am = oa;
+    }
+  }
+  float z = 0.f;
+  if (sampled) {
+    for (int t = lane; t < p.n_tiles; t += 32) {
+      const float tm = p.tstat_max[(long long)t * p.tstat_stride + m];
+      z += p.tstat_sum[(long long)t * p.tstat_stride + m] * expf((tm - mx) * p.inv_temp);
+    }
+    z = warp_sum(z);
+  }
+  if (lane == 0) {
+    *out_max = mx;
+    *out_z = z;
+    *out_arg = am == 0x7fffffff ? 0 : am;
+  }
+}
+
+// One verify round's acceptance and commit for sequence blockIdx.y.  Sampled
+// rounds run as a cluster of kDrawCluster CTAs that split the vocabulary for
+// the final draw; greedy rounds use one CTA.
+template <bool SAMPLED>
+__global__ void __launch_bounds__(kAccThreads) accept_round_kernel(const __grid_constant__ RoundAcceptParams p) {
+  __shared__ float s_max[kMaxWidth], s_z[kMaxWidth];
+  __shared__ int s_am[kMaxWidth];
+  __shared__ int s_n;
+  __shared__ unsigned long long s_scan[33];
+  __shared__ unsigned long long s_total;
+  pdl_wait();
+  pdl_launch_dependents();
+  const int b = blockIdx.y;
+  const int W = p.gamma + 1;
+  const int V = p.V;
+  const long long row0 = (long long)b * W;
+  const int warp = threadIdx.x >> 5;
+
+  if (warp < W) merge_row_stats(p, row0 + warp, SAMPLED, &s_max[warp], &s_z[warp], &s_am[warp]);
+  __syncthreads();
+
+  auto prob = [&](int row, int v) -> float {
+    return expf((p.logits[(row0 + row) * V + v] - s_max[row]) * p.inv_temp) / s_z[row];
+  };
+  auto xdraft = [&](int i) -> int { return p.tok[row0 + i]; };  // x_i = window row i
+
+  if (threadIdx.x == 0) {
+    int n = 0;
+    for (int i = 1; i <= p.gamma; ++i) {
+      const int x = xdraft(i);
+      bool acc;
+      if (x < 0 || x >= V) {
+        set_status(p.status, SPEC_ERR_INVALID_ARG);
+        acc = false;
+      } else if constexpr (SAMPLED) {
+        const float qx = p.q[((long long)b * p.gamma + (i - 1)) * V + x];
+        acc = __fmul_rn(p.u[row0 + i - 1], qx) < prob(i - 1, x);
+      } else {
+        acc = x == s_am[i - 1];
+      }
+      if (!acc) break;
+      ++n;
+    }
+    s_n = n;
+  }
+  __syncthreads();
+  const int n = s_n;
+
+  auto finish = [&](int tok_final) {  // one thread of the whole cluster
+    for (int j = 0; j < W; ++j) p.committed[row0 + j] = j < n ? xdraft(j + 1) : (j == n ? tok_final : -1);
+    p.accepted[b] = n;
+    p.bonus[b] = tok_final;
+    if (p.seq_ids) {
+      const int s = p.seq_ids[b];
+      if (s >= 0 && s < p.max_batch)
+        truncate_seq(s, min(p.seq_len[s] + 1 + n, p.max_pages * kPage), p.seq_len, p.seq_npages, p.page_table,
+                     p.max_pages, p.free_bits);
+    }
+  };
+
+  if constexpr (!SAMPLED) {
+    if (threadIdx.x == 0) finish(s_am[n]);
+    return;
+  } else {
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = (int)cluster.block_rank();
+    const int csize = (int)cluster.num_blocks();
+    const bool rejected = n < p.gamma;
+    const float* qn = rejected ? p.q + ((long long)b * p.gamma + n) * V : nullptr;
+    // this CTA's vocabulary slice, then this thread's sub-slice
+    const int slice = (V + csize - 1) / csize;
+    const int s0 = min(V, rank * slice), s1 = min(V, s0 + slice);
+    const int chunk = (s1 - s0 + kAccThreads - 1) / kAccThreads;
+    const int v0 = min(s1, s0 + (int)threadIdx.x * chunk), v1 = min(s1, v0 + chunk);
+    const unsigned long long m = (unsigned long long)floorf(p.u[row0 + p.gamma] * 16777216.0f);
+    unsigned long long* tot_remote[kMaxDrawCluster];
+    for (int pass = 0; pass < 2; ++pass) {
+      const bool use_resid = rejected && pass == 0;
+      auto mass = [&](int v) -> unsigned long long {
+        const float pv = prob(n, v);
+        const float r = use_resid ? fmaxf(0.f, pv - qn[v]) : pv;
+        return (unsigned long long)floorf(r * 1099511627776.0f);  // r * 2^40, exact
+      };
+      unsigned long long local = 0;
+      for (int v = v0; v < v1; ++v) local += mass(v);
+      unsigned long long cta_total;
+      const unsigned long long pre = block_exscan_u64(local, s_scan, &cta_total);
+      if (threadIdx.x == 0) s_total = cta_total;
+      cluster.sync();
+      unsigned long long S = 0, before = 0;
+      for (int r = 0; r < csize; ++r) {
+        tot_remote[r] = cluster.map_shared_rank(&s_total, r);
+        const unsigned long long tr = *tot_remote[r];
+        if (r < rank) before += tr;
+        S += tr;
+      }
+      cluster.sync();  // totals read before the next pass may overwrite them
+      if (S == 0ull) {
+        if (!use_resid) {  // p itself without mass on the grid: cannot happen for a distribution
+          if (rank == 0 && threadIdx.x == 0) finish(0);
+          break;
+        }
+        continue;  // residual without mass on the grid: draw from p at the same row
+      }
+      // t = floor(m * S / 2^24) with a 128-bit product (m < 2^24, S < 2^58)
+      const unsigned long long hi = __umul64hi(m, S), lo = m * S;
+      const unsigned long long t = (hi << 40) | (lo >> 24);
+      const unsigned long long gpre = before + pre;
+      if (local > 0 && gpre <= t && t < gpre + local) {
+        unsigned long long run = gpre;
+        for (int v = v0; v < v1; ++v) {
+          run += mass(v);
+          if (run > t) {
+            finish(v);
+            break;
+          }
+        }
+      }
+      break;
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kAccThreads) accept_tree_kernel(const __grid_constant__ TreeParams p) {
   __shared__ int s_path[kMaxWidth];
   __shared__ int s_n, s_tok;
@@ -261,10 +427,17 @@ __global__ void __launch_bounds__(kAccThreads) accept_tree_kernel(const __grid_c
   const int b = blockIdx.x;
   const int N = p.N;
   const long long row0 = (long long)b * N;
+  __shared__ float s_mx[kMaxWidth], s_z[kMaxWidth];
+  __shared__ int s_am[kMaxWidth];
+  {
+    const int warp = threadIdx.x >> 5;
+    if (warp < N) merge_row_stats(p.stats, row0 + warp, false, &s_mx[warp], &s_z[warp], &s_am[warp]);
+  }
+  __syncthreads();
   if (threadIdx.x == 0) {
     int v = 0, k = 0, a = 0;
     while (true) {
-      a = p.row_argmax[row0 + v];
+      a = s_am[v];
       int nxt = -1;
       for (int c = 1; c < N; ++c) {
         if (p.parent[c] == v && p.tok[row0 + c] == a) {
@@ -328,6 +501,12 @@ cudaError_t launch_accept_chain(const AcceptParams& p, bool sampled, PSource src
   if (!sampled) return launch_k(accept_chain_kernel<false, PSource::kLogits>, grid, block, 0, st, p);
   if (src == PSource::kProbs) return launch_k(accept_chain_kernel<true, PSource::kProbs>, grid, block, 0, st, p);
   return launch_k(accept_chain_kernel<true, PSource::kLogits>, grid, block, 0, st, p);
+}
+
+cudaError_t launch_accept_round(const RoundAcceptParams& p, bool sampled, cudaStream_t st) {
+  if (!sampled) return launch_k(accept_round_kernel<false>, dim3(1, p.B), dim3(kAccThreads), 0, st, p);
+  return launch_k_cluster(accept_round_kernel<true>, dim3(kDrawCluster, p.B), dim3(kAccThreads), 0, st,
+                          dim3(kDrawCluster, 1, 1), p);
 }
 
 cudaError_t launch_accept_tree(const TreeParams& p, cudaStream_t st) {

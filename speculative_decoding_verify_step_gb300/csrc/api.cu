@@ -107,11 +107,12 @@ struct spec_model {
   __nv_bfloat16 *xn = nullptr, *qrot = nullptr, *attn_out = nullptr, *act = nullptr;
   float* part = nullptr;
   long long part_elems = 0;
-  float *attn_acc = nullptr, *attn_ml = nullptr;
-  long long attn_slots = 0;  // capacity in (row*head*split) units
+  int* counters = nullptr;     // split-K tile counters (zero between launches)
+  float *ssq_a = nullptr, *ssq_b = nullptr;  // [d/128][M_max] partial sums of r^2
   float* logits = nullptr;
-  int32_t *row_pos = nullptr, *row_slot = nullptr, *seq_start = nullptr, *row_argmax = nullptr;
-  float *row_max = nullptr, *row_sum = nullptr;
+  float *tstat_max = nullptr, *tstat_sum = nullptr;  // [V/128][M_max] LM-head tile statistics
+  int32_t* tstat_arg = nullptr;
+  int32_t *row_pos = nullptr, *row_slot = nullptr, *seq_start = nullptr;
   float *rope_cos = nullptr, *rope_sin = nullptr;
   int32_t *scratch_ids = nullptr, *scratch_ids2 = nullptr, *scratch_tok = nullptr, *scratch_lens = nullptr;
   int32_t *scratch_acc = nullptr, *scratch_bonus = nullptr;
@@ -176,8 +177,11 @@ long long max_len_bound(const spec_model* m) {
 template <typename F>
 cudaError_t profiled(spec_model* m, int cls, double bytes, cudaStream_t st, F&& launch);
 
+// One target forward over B sequences x W rows.  depth[j]: position offset of row j;
+// anc[j]: rows visible to row j inside the window.  want_logits: run the LM head
+// (with per-tile softmax statistics at temperature 1/inv_temp when `sampled`).
 spec_status forward(spec_model* m, int B, int W, const int32_t* seq_ids, const int32_t* tok, const int* depth,
-                    const uint32_t* anc, bool want_logits, cudaStream_t st) {
+                    const uint32_t* anc, bool want_logits, bool sampled, float inv_temp, cudaStream_t st) {
   const spec_config& c = m->cfg;
   const int M = B * W;
   const int d = c.d_model, hd = c.head_dim;
@@ -203,8 +207,8 @@ spec_status forward(spec_model* m, int B, int W, const int32_t* seq_ids, const i
   pp.vocab = c.vocab;
   pp.status = m->status;
   CUDA_TRY(launch_prepare(pp, st));
-  CUDA_TRY(launch_embed_norm(tok, M, m->embed, m->layers[0].attn_norm, d, c.vocab, c.rms_eps, m->resid, m->xn,
-                             m->status, st));
+  CUDA_TRY(launch_embed(tok, M, m->embed, m->layers[0].attn_norm, d, c.vocab, m->resid, m->xn, m->ssq_a, m->M_max,
+                        m->status, st));
 
   const int BM = choose_bm(M);
   const int bi = bm_index(BM);
@@ -212,19 +216,15 @@ spec_status forward(spec_model* m, int B, int W, const int32_t* seq_ids, const i
     const long long cap = m->part_elems / ((long long)M * N);
     return choose_splits(N, K, M, BM, m->sm_count, (int)std::max(1LL, std::min(cap, 16LL)));
   };
-  const int s_qkv = splits_for(m->qkv_n, d);
-  const int s_o = splits_for(d, m->q_dim);
-  const int s_gu = splits_for(2 * F, d);
-  const int s_dn = splits_for(d, F);
-
-  // attention split-KV plan from the host-side length bound
-  const long long bound = std::min<long long>(max_len_bound(m) + W, c.max_seq_len);
-  const int pages_bound = (int)std::max<long long>(1, (bound + kPage - 1) / kPage);
-  int n_splits = std::max(1, (4 * m->sm_count) / std::max(1, B * Hkv));
-  n_splits = std::min(n_splits, pages_bound);
-  n_splits = (int)std::min<long long>(n_splits, std::max<long long>(1, m->attn_slots / ((long long)M * Hq)));
-  const int pps = (pages_bound + n_splits - 1) / n_splits;
-  n_splits = (pages_bound + pps - 1) / pps;
+  EpiParams base{};
+  base.M = M;
+  base.part = m->part;
+  base.counters = m->counters;
+  base.ssq_tiles = d / 128;
+  base.ssq_stride = m->M_max;
+  base.inv_d = 1.f / d;
+  base.eps = c.rms_eps;
+  base.status = m->status;
 
   AttnParams ap{};
   ap.q = m->qrot;
@@ -238,56 +238,126 @@ spec_status forward(spec_model* m, int B, int W, const int32_t* seq_ids, const i
   ap.Hq = Hq;
   ap.Hkv = Hkv;
   ap.hd = hd;
-  ap.pages_per_split = pps;
-  ap.n_splits = n_splits;
   for (int j = 0; j < 16; ++j) ap.anc[j] = j < W ? anc[j] : 0u;
-  ap.part_acc = m->attn_acc;
-  ap.part_ml = m->attn_ml;
+  ap.out = m->attn_out;
   ap.status = m->status;
 
   const long long layer_elems = (long long)c.num_pages * Hkv * kPage * hd;
   const double wb_qkv = 2.0 * m->qkv_n * d, wb_o = 2.0 * d * m->q_dim, wb_gu = 4.0 * F * d, wb_dn = 2.0 * d * F;
-  // K/V bytes one attention launch reads: the bound on the cached length (exact when known)
-  const double kv_bytes = 2.0 * 2.0 * hd * Hkv * (double)B * (double)std::min<long long>(bound, c.max_seq_len);
+  // K/V bytes of one attention launch: the host-side bound on the cached lengths
+  const long long bound = std::min<long long>(max_len_bound(m) + W, c.max_seq_len);
+  const double kv_bytes = 2.0 * 2.0 * hd * Hkv * (double)B * (double)bound;
   for (int l = 0; l < c.n_layers; ++l) {
     auto& Ly = m->layers[l];
-    CUDA_TRY(profiled(m, 0, wb_qkv, st, [&] {
-      return launch_gemm(&Ly.tm_qkv, &m->tm_xn[bi], BM, m->qkv_n, d, M, s_qkv, m->part, (long long)M * m->qkv_n,
-                         m->qkv_n, m->status, st);
-    }));
-    CUDA_TRY(launch_qkv_epilogue(m->part, s_qkv, (long long)M * m->qkv_n, M, Hq, Hkv, hd, m->row_pos, m->row_slot,
-                                 m->rope_cos, m->rope_sin, m->qrot, m->kpool + l * layer_elems,
-                                 m->vpool + l * layer_elems, st));
+    {
+      EpiParams e = base;
+      e.N = m->qkv_n;
+      e.K = d;
+      e.splits = splits_for(e.N, e.K);
+      e.split_stride = (long long)M * e.N;
+      e.ssq_in = m->ssq_a;
+      e.Hq = Hq;
+      e.Hkv = Hkv;
+      e.hd = hd;
+      e.row_pos = m->row_pos;
+      e.row_slot = m->row_slot;
+      e.rope_cos = m->rope_cos;
+      e.rope_sin = m->rope_sin;
+      e.q_out = m->qrot;
+      e.kpool = m->kpool + l * layer_elems;
+      e.vpool = m->vpool + l * layer_elems;
+      CUDA_TRY(profiled(m, 0, wb_qkv, st, [&] { return launch_gemm_epi(kEpiQKV, &Ly.tm_qkv, &m->tm_xn[bi], BM, e, st); }));
+    }
     ap.layer_row0 = l * c.num_pages * Hkv * kPage;
-    CUDA_TRY(profiled(m, 5, kv_bytes, st, [&] {
-      cudaError_t e = launch_attention(&m->tm_k, &m->tm_v, ap, st);
-      if (e != cudaSuccess) return e;
-      return launch_attn_merge(m->attn_acc, m->attn_ml, M, Hq, hd, n_splits, m->attn_out, st);
-    }));
-    CUDA_TRY(profiled(m, 1, wb_o, st, [&] {
-      return launch_gemm(&Ly.tm_o, &m->tm_attn[bi], BM, d, m->q_dim, M, s_o, m->part, (long long)M * d, d,
-                         m->status, st);
-    }));
-    CUDA_TRY(launch_resid_norm(m->part, s_o, (long long)M * d, M, d, Ly.ffn_norm, c.rms_eps, m->resid, m->xn, st));
-    CUDA_TRY(profiled(m, 2, wb_gu, st, [&] {
-      return launch_gemm(&Ly.tm_gu, &m->tm_xn[bi], BM, 2 * F, d, M, s_gu, m->part, (long long)M * 2 * F, 2 * F,
-                         m->status, st);
-    }));
-    CUDA_TRY(launch_swiglu(m->part, s_gu, (long long)M * 2 * F, M, F, m->act, st));
-    CUDA_TRY(profiled(m, 3, wb_dn, st, [&] {
-      return launch_gemm(&Ly.tm_down, &m->tm_act[bi], BM, d, F, M, s_dn, m->part, (long long)M * d, d, m->status,
-                         st);
-    }));
-    const float* next_gain = l + 1 < c.n_layers ? m->layers[l + 1].attn_norm : m->final_norm;
-    CUDA_TRY(launch_resid_norm(m->part, s_dn, (long long)M * d, M, d, next_gain, c.rms_eps, m->resid, m->xn, st));
+    CUDA_TRY(profiled(m, 5, kv_bytes, st, [&] { return launch_attention(&m->tm_k, &m->tm_v, ap, st); }));
+    {
+      EpiParams e = base;
+      e.N = d;
+      e.K = m->q_dim;
+      e.splits = splits_for(e.N, e.K);
+      e.split_stride = (long long)M * e.N;
+      e.ssq_in = nullptr;
+      e.resid = m->resid;
+      e.g_next = Ly.ffn_norm;
+      e.xn = m->xn;
+      e.ssq_out = m->ssq_b;
+      e.d = d;
+      CUDA_TRY(profiled(m, 1, wb_o, st, [&] { return launch_gemm_epi(kEpiResid, &Ly.tm_o, &m->tm_attn[bi], BM, e, st); }));
+    }
+    {
+      EpiParams e = base;
+      e.N = 2 * F;
+      e.K = d;
+      e.splits = splits_for(e.N, e.K);
+      e.split_stride = (long long)M * e.N;
+      e.ssq_in = m->ssq_b;
+      e.act = m->act;
+      e.ffn = F;
+      CUDA_TRY(profiled(m, 2, wb_gu, st, [&] { return launch_gemm_epi(kEpiSwiGLU, &Ly.tm_gu, &m->tm_xn[bi], BM, e, st); }));
+    }
+    {
+      EpiParams e = base;
+      e.N = d;
+      e.K = F;
+      e.splits = splits_for(e.N, e.K);
+      e.split_stride = (long long)M * e.N;
+      e.ssq_in = nullptr;
+      e.resid = m->resid;
+      e.g_next = l + 1 < c.n_layers ? m->layers[l + 1].attn_norm : m->final_norm;
+      e.xn = m->xn;
+      e.ssq_out = m->ssq_a;
+      e.d = d;
+      CUDA_TRY(profiled(m, 3, wb_dn, st, [&] { return launch_gemm_epi(kEpiResid, &Ly.tm_down, &m->tm_act[bi], BM, e, st); }));
+    }
   }
   if (want_logits) {
-    CUDA_TRY(profiled(m, 4, 2.0 * c.vocab * d, st, [&] {
-      return launch_gemm(&m->tm_lm, &m->tm_xn[bi], BM, c.vocab, d, M, 1, m->logits, 0, c.vocab, m->status, st);
-    }));
+    EpiParams e = base;
+    e.N = c.vocab;
+    e.K = d;
+    e.splits = 1;
+    e.split_stride = 0;
+    e.ssq_in = m->ssq_a;
+    e.logits = m->logits;
+    e.inv_temp = inv_temp;
+    e.tstat_max = m->tstat_max;
+    e.tstat_sum = sampled ? m->tstat_sum : nullptr;
+    e.tstat_arg = m->tstat_arg;
+    e.tstat_stride = m->M_max;
+    CUDA_TRY(profiled(m, 4, 2.0 * c.vocab * d, st, [&] { return launch_gemm_epi(kEpiLogits, &m->tm_lm, &m->tm_xn[bi], BM, e, st); }));
     m->last_rows = M;
   }
   return SPEC_OK;
+}
+
+RoundAcceptParams round_params(spec_model* m, int B, int gamma, const int32_t* seq_ids, const int32_t* tok,
+                               const float* q, const float* u, float inv_temp, int32_t* accepted,
+                               int32_t* committed, int32_t* bonus) {
+  RoundAcceptParams r{};
+  r.B = B;
+  r.gamma = gamma;
+  r.V = m->cfg.vocab;
+  r.inv_temp = inv_temp;
+  r.logits = m->logits;
+  r.n_tiles = m->cfg.vocab / 128;
+  r.tstat_max = m->tstat_max;
+  r.tstat_sum = m->tstat_sum;
+  r.tstat_arg = m->tstat_arg;
+  r.tstat_stride = m->M_max;
+  r.q = q;
+  r.tok = tok;
+  r.u = u;
+  r.accepted = accepted;
+  r.committed = committed;
+  r.bonus = bonus;
+  r.seq_ids = seq_ids;
+  r.seq_len = m->seq_len;
+  r.seq_npages = m->seq_npages;
+  r.page_table = m->page_table;
+  r.free_bits = m->free_bits;
+  r.max_pages = m->max_pages;
+  r.max_batch = m->cfg.max_batch;
+  r.status = m->status;
+  return r;
 }
 
 constexpr int kProfMax = 1024;
@@ -418,18 +488,16 @@ spec_status spec_model_create(const spec_config* cfg, spec_model** out) {
   m->part_elems = std::max<long long>((long long)M_max * std::max({m->qkv_n, 2 * F, d}),
                                       16LL * std::min(M_max, 64) * std::max({m->qkv_n, 2 * F, d}));
   ALLOC(m->part, m->part_elems);
-  const int grp = c.n_heads / c.n_kv_heads;
-  m->attn_slots = (long long)(4 * m->sm_count / c.n_kv_heads + c.max_batch + 1) * c.max_width * grp * c.n_kv_heads;
-  m->attn_slots = std::max<long long>(m->attn_slots, (long long)M_max * c.n_heads);
-  ALLOC(m->attn_acc, (size_t)m->attn_slots * hd);
-  ALLOC(m->attn_ml, (size_t)m->attn_slots * 2);
+  ALLOC(m->counters, (size_t)(std::max({m->qkv_n, 2 * F, d}) / 128) * ((M_max + 7) / 8));
+  ALLOC(m->ssq_a, (size_t)(d / 128) * M_max);
+  ALLOC(m->ssq_b, (size_t)(d / 128) * M_max);
   ALLOC(m->logits, (size_t)M_max * V);
+  ALLOC(m->tstat_max, (size_t)(V / 128) * M_max);
+  ALLOC(m->tstat_sum, (size_t)(V / 128) * M_max);
+  ALLOC(m->tstat_arg, (size_t)(V / 128) * M_max);
   ALLOC(m->row_pos, M_max);
   ALLOC(m->row_slot, M_max);
   ALLOC(m->seq_start, c.max_batch);
-  ALLOC(m->row_argmax, M_max);
-  ALLOC(m->row_max, M_max);
-  ALLOC(m->row_sum, M_max);
   ALLOC(m->rope_cos, (size_t)c.max_seq_len * (hd / 2));
   ALLOC(m->rope_sin, (size_t)c.max_seq_len * (hd / 2));
   ALLOC(m->scratch_ids, c.max_batch);
@@ -616,7 +684,7 @@ spec_status spec_prefill(spec_model* m, int32_t B, const int32_t* seq_ids, const
     chain_masks(W, depth, anc);
     CUDA_TRY(launch_gather_tokens(tokens, stride, m->scratch_lens, k, c0, W, m->scratch_tok, seq_ids, m->scratch_ids2,
                                   st));
-    if (auto s = forward(m, k, W, m->scratch_ids2, m->scratch_tok, depth, anc, false, st)) return s;
+    if (auto s = forward(m, k, W, m->scratch_ids2, m->scratch_tok, depth, anc, false, false, 1.f, st)) return s;
     CUDA_TRY(launch_commit_all(m->scratch_ids2, k, W, m->cfg.max_batch, m->seq_len, st));
   }
   for (int i = 0; i < B; ++i) {  // the ragged tail of each prompt
@@ -627,7 +695,7 @@ spec_status spec_prefill(spec_model* m, int32_t B, const int32_t* seq_ids, const
     chain_masks(r, depth, anc);
     CUDA_TRY(launch_gather_tokens(tokens, stride, m->scratch_lens + i, 1, c0, r, m->scratch_tok, seq_ids,
                                   m->scratch_ids2, st));
-    if (auto s = forward(m, 1, r, m->scratch_ids2, m->scratch_tok, depth, anc, false, st)) return s;
+    if (auto s = forward(m, 1, r, m->scratch_ids2, m->scratch_tok, depth, anc, false, false, 1.f, st)) return s;
     CUDA_TRY(launch_commit_all(m->scratch_ids2, 1, r, m->cfg.max_batch, m->seq_len, st));
   }
   m->last_launches = g_launch_count;
@@ -650,7 +718,7 @@ spec_status spec_score(spec_model* m, int32_t B, int32_t W, const int32_t* seq_i
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   g_launch_count = 0;
-  if (auto s = forward(m, B, W, seq_ids, tok, depth, anc, true, st)) return s;
+  if (auto s = forward(m, B, W, seq_ids, tok, depth, anc, true, false, 1.f, st)) return s;
   if (logits_out)
     CUDA_TRY(cudaMemcpyAsync(logits_out, m->logits, (size_t)B * W * m->cfg.vocab * 4, cudaMemcpyDeviceToDevice, st));
   m->last_launches = g_launch_count;
@@ -670,34 +738,11 @@ spec_status spec_decode_step(spec_model* m, int32_t B, const int32_t* seq_ids, c
   uint32_t anc[16];
   chain_masks(1, depth, anc);
   g_launch_count = 0;
-  if (auto s = forward(m, B, 1, seq_ids, tok, depth, anc, true, st)) return s;
   const float inv_t = sampled ? 1.f / temperature : 1.f;
-  CUDA_TRY(launch_row_stats(m->logits, B, m->cfg.vocab, inv_t, sampled, m->row_argmax, m->row_max, m->row_sum, st));
-  AcceptParams ap{};
-  ap.B = B;
-  ap.gamma = 0;
-  ap.V = m->cfg.vocab;
-  ap.inv_temp = inv_t;
-  ap.rows = m->logits;
-  ap.tok = tok;
-  ap.tok_stride = 1;
-  ap.tok_offset = 1;
-  ap.u = u;
-  ap.row_argmax = m->row_argmax;
-  ap.row_max = m->row_max;
-  ap.row_sum = m->row_sum;
-  ap.accepted = m->scratch_acc;
-  ap.committed = next_tok;
-  ap.bonus = m->scratch_bonus;
-  ap.seq_ids = seq_ids;
-  ap.seq_len = m->seq_len;
-  ap.seq_npages = m->seq_npages;
-  ap.page_table = m->page_table;
-  ap.free_bits = m->free_bits;
-  ap.max_pages = m->max_pages;
-  ap.max_batch = m->cfg.max_batch;
-  ap.status = m->status;
-  CUDA_TRY(launch_accept_chain(ap, sampled, PSource::kLogits, st));
+  if (auto s = forward(m, B, 1, seq_ids, tok, depth, anc, true, sampled, inv_t, st)) return s;
+  RoundAcceptParams rp = round_params(m, B, 0, seq_ids, tok, nullptr, u, inv_t, m->scratch_acc, next_tok,
+                                      m->scratch_bonus);
+  CUDA_TRY(launch_accept_round(rp, sampled, st));
   bump_bounds(m, 1);
   m->last_launches = g_launch_count;
   return SPEC_OK;
@@ -720,36 +765,10 @@ spec_status spec_verify_step(spec_model* m, int32_t B, int32_t gamma, const int3
   uint32_t anc[16];
   chain_masks(W, depth, anc);
   g_launch_count = 0;
-  if (auto s = forward(m, B, W, seq_ids, tok, depth, anc, true, st)) return s;
   const float inv_t = sampled ? 1.f / temperature : 1.f;
-  CUDA_TRY(launch_row_stats(m->logits, B * W, m->cfg.vocab, inv_t, sampled, m->row_argmax, m->row_max, m->row_sum,
-                            st));
-  AcceptParams ap{};
-  ap.B = B;
-  ap.gamma = gamma;
-  ap.V = m->cfg.vocab;
-  ap.inv_temp = inv_t;
-  ap.rows = m->logits;
-  ap.q = q;
-  ap.tok = tok;
-  ap.tok_stride = W;
-  ap.tok_offset = 1;
-  ap.u = u;
-  ap.row_argmax = m->row_argmax;
-  ap.row_max = m->row_max;
-  ap.row_sum = m->row_sum;
-  ap.accepted = accepted;
-  ap.committed = committed;
-  ap.bonus = bonus;
-  ap.seq_ids = seq_ids;
-  ap.seq_len = m->seq_len;
-  ap.seq_npages = m->seq_npages;
-  ap.page_table = m->page_table;
-  ap.free_bits = m->free_bits;
-  ap.max_pages = m->max_pages;
-  ap.max_batch = m->cfg.max_batch;
-  ap.status = m->status;
-  CUDA_TRY(launch_accept_chain(ap, sampled, PSource::kLogits, st));
+  if (auto s = forward(m, B, W, seq_ids, tok, depth, anc, true, sampled, inv_t, st)) return s;
+  RoundAcceptParams rp = round_params(m, B, gamma, seq_ids, tok, q, u, inv_t, accepted, committed, bonus);
+  CUDA_TRY(launch_accept_round(rp, sampled, st));
   bump_bounds(m, W);
   m->last_launches = g_launch_count;
   return SPEC_OK;
@@ -766,16 +785,14 @@ spec_status spec_verify_tree_step(spec_model* m, int32_t B, int32_t n_nodes, con
   if (auto s = tree_masks(n_nodes, parent_host, depth, anc)) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   g_launch_count = 0;
-  if (auto s = forward(m, B, n_nodes, seq_ids, tok, depth, anc, true, st)) return s;
-  CUDA_TRY(launch_row_stats(m->logits, B * n_nodes, m->cfg.vocab, 1.f, false, m->row_argmax, m->row_max, m->row_sum,
-                            st));
+  if (auto s = forward(m, B, n_nodes, seq_ids, tok, depth, anc, true, false, 1.f, st)) return s;
   TreeParams tp{};
   tp.B = B;
   tp.N = n_nodes;
+  tp.stats = round_params(m, B, n_nodes - 1, seq_ids, tok, nullptr, nullptr, 1.f, accepted, committed, bonus);
   tp.V = m->cfg.vocab;
   for (int j = 0; j < 16; ++j) tp.parent[j] = j < n_nodes ? parent_host[j] : -1;
   tp.tok = tok;
-  tp.row_argmax = m->row_argmax;
   tp.accepted = accepted;
   tp.committed = committed;
   tp.bonus = bonus;

@@ -15,27 +15,59 @@ extern bool g_use_pdl;
 // Message for spec_last_error() (thread-local), for entry points outside api.cu.
 void record_error(const char* msg);
 
-// Y_partial[split][m][n] = sum_{k in split} X[m][k] * W[n][k]
-// tmW: weight map, box {64, 128}; tmX: activation map, box {64, BM}; BM in {8,16,32,64}.
-// splits == 1 writes the final result (out[m*ldo + n]).
-cudaError_t launch_gemm(const CUtensorMap* tmW, const CUtensorMap* tmX, int BM, int N, int K, int M, int splits,
-                        float* out, long long split_stride, int ldo, int* status, cudaStream_t st);
+// Fused-epilogue projection (gemm.cu).  Y = X W^T over M rows; W: [N, K] bf16
+// (tensor map box {64, 128}), X: [M_alloc, K] bf16 (box {64, BM}, BM in 8/16/32/64).
+// split-K partials land in `part` ([splits][M][N] fp32); the last split CTA of a
+// tile reduces them and applies the epilogue:
+enum { kEpiQKV = 0, kEpiSwiGLU = 1, kEpiResid = 2, kEpiLogits = 3 };
+struct EpiParams {
+  int M, N, K;
+  int kb_total, kb_per_split, splits;  // kb_* filled by the launcher
+  float* part;
+  long long split_stride;
+  int* counters;                       // one per (m tile, n tile), zero between launches
+  // row scale of a normalised input (ssq_in = null: scale 1)
+  const float* ssq_in;                 // [ssq_tiles][ssq_stride] partial sums of r^2
+  int ssq_tiles, ssq_stride;
+  float inv_d, eps;
+  // kEpiQKV: RoPE + q out + paged K/V write
+  int Hq, Hkv, hd;
+  const int32_t* row_pos;
+  const int32_t* row_slot;
+  const float* rope_cos;
+  const float* rope_sin;
+  __nv_bfloat16* q_out;
+  __nv_bfloat16* kpool;                // this layer's base
+  __nv_bfloat16* vpool;
+  // kEpiSwiGLU
+  __nv_bfloat16* act;
+  int ffn;
+  // kEpiResid: resid += y, xn = bf16(resid * g_next), ssq_out partial sums
+  float* resid;
+  const float* g_next;
+  __nv_bfloat16* xn;
+  float* ssq_out;
+  int d;
+  // kEpiLogits: logits and per-128-column (max, sum exp((l-max)/T), argmax) of each row
+  float* logits;
+  float inv_temp;
+  float* tstat_max;
+  float* tstat_sum;                    // null: greedy (no sum)
+  int32_t* tstat_arg;
+  int tstat_stride;
+  int* status;
+};
+cudaError_t launch_gemm_epi(int epi, const CUtensorMap* tmW, const CUtensorMap* tmX, int BM, EpiParams p,
+                            cudaStream_t st);
 
 // Choose split-K for an N x K projection over M rows so that the grid fills the GPU.
 int choose_splits(int N, int K, int M, int BM, int sm_count, int max_splits);
 int choose_bm(int M);
 
-// --- elementwise (elementwise.cu)
-cudaError_t launch_embed_norm(const int32_t* tok, int M, const __nv_bfloat16* embed, const float* gain, int d,
-                              int vocab, float eps, float* resid, __nv_bfloat16* xn, int* status, cudaStream_t st);
-cudaError_t launch_qkv_epilogue(const float* part, int splits, long long split_stride, int M, int n_heads,
-                                int n_kv, int hd, const int32_t* row_pos, const int32_t* row_slot,
-                                const float* rope_cos, const float* rope_sin, __nv_bfloat16* q_out,
-                                __nv_bfloat16* kpool_layer, __nv_bfloat16* vpool_layer, cudaStream_t st);
-cudaError_t launch_resid_norm(const float* part, int splits, long long split_stride, int M, int d, const float* gain,
-                              float eps, float* resid, __nv_bfloat16* xn, cudaStream_t st);
-cudaError_t launch_swiglu(const float* part, int splits, long long split_stride, int M, int ffn,
-                          __nv_bfloat16* act, cudaStream_t st);
+// --- elementwise (elementwise.cu): resid = E[tok]; xn = bf16(E[tok] * g); ssq partials
+cudaError_t launch_embed(const int32_t* tok, int M, const __nv_bfloat16* embed, const float* gain, int d, int vocab,
+                         float* resid, __nv_bfloat16* xn, float* ssq_out, int ssq_stride, int* status,
+                         cudaStream_t st);
 
 // --- attention (attention.cu)
 struct AttnParams {
@@ -46,15 +78,13 @@ struct AttnParams {
   int max_pages, max_batch;
   int B, W, Hq, Hkv, hd;
   int layer_row0;              // first TMA row of this layer in the KV pool maps
-  int pages_per_split, n_splits;
+  int pages_per_split;         // pages per CTA; the cluster of kAttnCluster CTAs covers a sequence
   uint32_t anc[16];            // ancestor masks of the window rows (bit i: row i visible)
-  float* part_acc;             // [M*Hq, n_splits, hd]
-  float* part_ml;              // [M*Hq, n_splits, 2]
+  __nv_bfloat16* out;          // [M, Hq*hd]
   int* status;
 };
+constexpr int kAttnCluster = 8;
 cudaError_t launch_attention(const CUtensorMap* tmK, const CUtensorMap* tmV, const AttnParams& p, cudaStream_t st);
-cudaError_t launch_attn_merge(const float* part_acc, const float* part_ml, int M, int Hq, int hd, int n_splits,
-                              __nv_bfloat16* out, cudaStream_t st);
 
 // --- sequence state, acceptance and commit (accept.cu)
 struct PrepareParams {
@@ -104,11 +134,39 @@ cudaError_t launch_row_stats(const float* rows, int n_rows, int V, float inv_tem
                              float* row_max, float* row_sum, cudaStream_t st);
 cudaError_t launch_accept_chain(const AcceptParams& p, bool sampled, PSource src, cudaStream_t st);
 
+// Acceptance of a model round from the LM head's per-tile statistics.
+constexpr int kDrawCluster = 8;
+constexpr int kMaxDrawCluster = 16;
+struct RoundAcceptParams {
+  int B, gamma, V;
+  float inv_temp;
+  const float* logits;       // [B*W, V]
+  int n_tiles;               // V / 128
+  const float* tstat_max;    // [n_tiles][tstat_stride]
+  const float* tstat_sum;
+  const int32_t* tstat_arg;
+  int tstat_stride;
+  const float* q;            // [B, gamma, V] (sampled)
+  const int32_t* tok;        // [B, W] window tokens
+  const float* u;            // [B, W] (sampled)
+  int32_t* accepted;
+  int32_t* committed;        // [B, W]
+  int32_t* bonus;
+  const int32_t* seq_ids;    // null: no commit
+  int32_t* seq_len;
+  int32_t* seq_npages;
+  int32_t* page_table;
+  uint32_t* free_bits;
+  int max_pages, max_batch;
+  int* status;
+};
+cudaError_t launch_accept_round(const RoundAcceptParams& p, bool sampled, cudaStream_t st);
+
 struct TreeParams {
   int B, N, V;
   int parent[16];
   const int32_t* tok;        // [B, N]
-  const int32_t* row_argmax; // [B*N]
+  RoundAcceptParams stats;   // tile statistics of the B*N node rows (greedy)
   int32_t* accepted;
   int32_t* committed;        // [B, N]
   int32_t* bonus;
