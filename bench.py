@@ -59,6 +59,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-lam-sweep", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the batch sweep, the 32K-context and the tree workloads")
     ap.add_argument("--cpu-layers", type=int, default=2, help="layers in the oracle's timed sample")
     ap.add_argument("--quick", action="store_true", help="a short run for profilers: timed replay only")
     ap.add_argument("--ncu", action="store_true",
@@ -146,10 +148,13 @@ class Bench:
         self.dims = synth.LLAMA8B.with_layers(args.layers)
         B, ctx = args.batch, args.ctx
         self.B = B
-        self.max_seq = ctx + 64 * 32
-        pages_per_seq = -(-self.max_seq // 64)
-        self.model = spec.SpecModel(self.dims, max_batch=B, max_width=16, max_seq_len=self.max_seq,
-                                    num_pages=B * pages_per_seq + 8)
+        # one model sized for every workload: 64 sequence slots, 32K-token contexts
+        self.max_batch = max(B, 64)
+        self.max_seq = max(ctx + 64 * 32, 32768 + 1024)
+        self.num_pages = max(B * (-(-(ctx + 64 * 32) // 64)), 8 * (-(-self.max_seq // 64)) + 64,
+                             64 * (2048 + 1024) // 64) + 8
+        self.model = spec.SpecModel(self.dims, max_batch=self.max_batch, max_width=16, max_seq_len=self.max_seq,
+                                    num_pages=self.num_pages)
         self.model.load_weights(synth.iter_weights(self.dims, seed=1, device=device))
         torch.cuda.synchronize()
         self.ids = torch.arange(B, dtype=torch.int32, device=device)
@@ -322,6 +327,86 @@ class Bench:
                 t_dec = ms
             res[W] = ms
         return {str(W): {"ms": round(ms, 4), "ratio_to_decode": round(ms / t_dec, 4)} for W, ms in res.items()}
+
+    def timed_rounds(self, B, W, lens, steps, warmup, tree=None, temp=1.0):
+        """Mean ms of a round (W = 1: decode step) for B sequences whose caches hold
+        `lens` tokens of random KV.  Sampled rounds use drafts that get rejected (q
+        one-hot on a random token) so the cache grows one token per round; tree
+        rounds are greedy over the given parent list."""
+        torch = self.torch
+        V = self.dims.vocab
+        ids = list(range(B))
+        self.model.kv_fill_random(ids, lens, seed=11, scale=0.5)
+        dids = torch.arange(B, dtype=torch.int32, device=self.dev)
+        g = torch.Generator(device=self.dev)
+        g.manual_seed(19)
+        tok = torch.randint(0, V, (B, W), generator=g, device=self.dev, dtype=torch.int64).int()
+        outs = (torch.empty(B, dtype=torch.int32, device=self.dev), torch.empty(B, W, dtype=torch.int32,
+                                                                                device=self.dev),
+                torch.empty(B, dtype=torch.int32, device=self.dev))
+        if tree is not None:
+            run = lambda: self.model.verify_tree_step(dids, tok, tree, outs=outs)
+        elif W == 1:
+            u = torch.full((B,), 0.5, device=self.dev)
+            run = lambda: self.model.decode_step(dids, tok[:, 0], temperature=temp, u=u, out=outs[0])
+        else:
+            q = torch.zeros(B, W - 1, V, device=self.dev)
+            q.scatter_(2, tok[:, 1:].long().unsqueeze(-1), 1.0)
+            u = torch.full((B, W), 0.5, device=self.dev)
+            run = lambda: self.model.verify_step(dids, tok, q=q, u=u, temperature=temp, outs=outs)
+        for _ in range(warmup):
+            run()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            run()
+        e1.record()
+        torch.cuda.synchronize()
+        self.model.sync_status()
+        self.model.seq_reset(ids)
+        return e0.elapsed_time(e1) / steps
+
+    def workloads(self, steps, warmup, hbm_peak):
+        """The batch sweep, the 32K-context rounds and the tree rounds."""
+        wb = weight_bytes(self.dims)
+        kv_tok = 4.0 * self.dims.n_kv_heads * self.dims.head_dim * self.dims.n_layers  # K+V bytes per token
+        out = {}
+        lens_all = self.synth.prompt_lengths(64, 512, 2048, seed=5).tolist()
+        sweep = {}
+        for B in (1, 4, 16, 64):
+            lens = lens_all[:B]
+            t_dec = self.timed_rounds(B, 1, lens, steps, warmup)
+            t_ver = self.timed_rounds(B, 5, lens, steps, warmup)
+            by = wb + kv_tok * (sum(lens) + 5 * B)
+            sweep[str(B)] = {"verify_ms": round(t_ver, 4), "decode_ms": round(t_dec, 4),
+                             "t_verify_over_t_decode": round(t_ver / t_dec, 4),
+                             "rows": 5 * B, "algorithmic_GB": round(by / 1e9, 3),
+                             "achieved_GBps": round(by / (t_ver / 1000) / 1e9, 1),
+                             "frac_of_peak": round(by / (t_ver / 1000) / 1e9 / hbm_peak, 4)}
+        out["batch_sweep_w5_ctx512_2048"] = sweep
+        lc = {}
+        lens = [32768] * 8
+        t_dec = self.timed_rounds(8, 1, lens, steps, warmup)
+        lc["decode_ms"] = round(t_dec, 4)
+        for gamma in (3, 7):
+            t = self.timed_rounds(8, gamma + 1, lens, steps, warmup)
+            by = wb + kv_tok * 8 * (32768 + gamma + 1)
+            lc[f"gamma{gamma}"] = {"verify_ms": round(t, 4), "t_verify_over_t_decode": round(t / t_dec, 4),
+                                   "algorithmic_GB": round(by / 1e9, 3),
+                                   "achieved_GBps": round(by / (t / 1000) / 1e9, 1),
+                                   "frac_of_peak": round(by / (t / 1000) / 1e9 / hbm_peak, 4)}
+        out["long_context_b8_ctx32768"] = lc
+        tree = [-1, 0, 0, 1, 1, 2, 2, 3, 3, 4, 4, 5, 5, 6, 6]
+        lens = [4096] * 4
+        t_dec = self.timed_rounds(4, 1, lens, steps, warmup, temp=0.0)
+        t = self.timed_rounds(4, len(tree), lens, steps, warmup, tree=tree)
+        by = wb + kv_tok * 4 * (4096 + len(tree))
+        out["tree15_b4_ctx4096"] = {"verify_ms": round(t, 4), "decode_ms": round(t_dec, 4),
+                                    "t_verify_over_t_decode": round(t / t_dec, 4), "rows": 60,
+                                    "achieved_GBps": round(by / (t / 1000) / 1e9, 1),
+                                    "frac_of_peak": round(by / (t / 1000) / 1e9 / hbm_peak, 4)}
+        return out
 
     def _barrier(self):
         torch = self.torch
@@ -516,7 +601,7 @@ def main():
 
     out = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
-           "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+           "scaling": "weak", "vs_baseline": None, "dtype": "f16",
            "data": "synthetic: random-init N(0,0.02) bf16 weights, random-token prompts, drafts from "
                    "q=(1-lam)p+lam*Dir(1) with p the target at the draft prefix",
            "config": {"workload": f"llama3.1-8b-shape ({args.layers} layers) sampled verify round, "
@@ -581,6 +666,8 @@ def main():
                                     "accepted_tok_s_at_headline_step_time": round(args.batch * tpr / (ms_per_step
                                                                                                      / 1000), 2)}
             out["lam_sweep"] = lam_res
+        if not args.no_configs:
+            out["workloads"] = b.workloads(max(5, min(args.steps, 20)), 3, hbm_peak)
         if rank == 0 and not args.no_cpu_baseline:
             t_start = time.perf_counter()
             smp = OracleSample(args)

@@ -189,8 +189,9 @@ spec_status spec_accept_greedy_noalloc(int32_t B, int32_t gamma, int32_t V, cons
 spec_status spec_get_kv_state(spec_model* m, int32_t n, const int32_t* seq_ids_host, int32_t* seq_len_host,
                               int32_t* page_table_host);
 
-/* Synchronous host copy of cached K and V (bf16 bits) of one sequence, slots
- * [t0, t0+n), layer `layer`: k_host and v_host are [n, n_kv_heads, head_dim] uint16. */
+/* Synchronous host copy of cached K and V (fp16 bits: the cache is fp16) of one
+ * sequence, slots [t0, t0+n), layer `layer`: k_host and v_host are
+ * [n, n_kv_heads, head_dim] uint16. */
 spec_status spec_read_kv(spec_model* m, int32_t layer, int32_t seq_id, int32_t t0, int32_t n,
                          uint16_t* k_host, uint16_t* v_host);
 

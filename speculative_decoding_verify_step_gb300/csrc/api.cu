@@ -60,7 +60,7 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   return fn;
 }
 
-// 2-D bf16 map over a row-major [outer, inner] array, 128-byte swizzle.
+// 2-D fp16 map over a row-major [outer, inner] array, 128-byte swizzle.
 bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
               uint32_t box_outer) {
   auto enc = get_encode();
@@ -69,13 +69,18 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer
   cuuint64_t strides[1] = {inner * 2};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-constexpr int kBMs[4] = {8, 16, 32, 64};
-int bm_index(int bm) { return bm == 8 ? 0 : bm == 16 ? 1 : bm == 32 ? 2 : 3; }
+constexpr int kNumBM = 6;
+constexpr int kBMs[kNumBM] = {8, 16, 32, 64, 128, 256};
+int bm_index(int bm) {
+  for (int i = 0; i < kNumBM; ++i)
+    if (kBMs[i] == bm) return i;
+  return 0;
+}
 
 }  // namespace
 
@@ -85,17 +90,20 @@ struct spec_model {
   int max_pages = 0, M_max = 0, qkv_n = 0, q_dim = 0, kv_dim = 0;
   std::vector<void*> allocs;
   // weights
-  __nv_bfloat16 *embed = nullptr, *lm_head = nullptr;
+  __nv_bfloat16* embed = nullptr;  // gathered, kept bf16
+  act_t* lm_head = nullptr;        // projections: fp16 re-encoding with a per-row scale
+  float* rs_lm = nullptr;
   float* final_norm = nullptr;
   struct Layer {
-    __nv_bfloat16 *wqkv, *wo, *wgu, *wdown;
+    act_t *wqkv, *wo, *wgu, *wdown;
+    float *rs_qkv, *rs_o, *rs_gu, *rs_down;
     float *attn_norm, *ffn_norm;
     CUtensorMap tm_qkv, tm_o, tm_gu, tm_down;
   };
   std::vector<Layer> layers;
   CUtensorMap tm_lm;
   // KV pool: [layer][page][kv head][64][head_dim] for K and for V
-  __nv_bfloat16 *kpool = nullptr, *vpool = nullptr;
+  act_t *kpool = nullptr, *vpool = nullptr;
   CUtensorMap tm_k, tm_v;
   // sequence state
   int32_t *seq_len = nullptr, *seq_npages = nullptr, *page_table = nullptr;
@@ -104,7 +112,7 @@ struct spec_model {
   std::vector<long long> host_len_bound;
   // workspaces
   float* resid = nullptr;
-  __nv_bfloat16 *xn = nullptr, *qrot = nullptr, *attn_out = nullptr, *act = nullptr;
+  act_t *xn = nullptr, *qrot = nullptr, *attn_out = nullptr, *act = nullptr;
   float* part = nullptr;
   long long part_elems = 0;
   int* counters = nullptr;     // split-K tile counters (zero between launches)
@@ -116,7 +124,8 @@ struct spec_model {
   float *rope_cos = nullptr, *rope_sin = nullptr;
   int32_t *scratch_ids = nullptr, *scratch_ids2 = nullptr, *scratch_tok = nullptr, *scratch_lens = nullptr;
   int32_t *scratch_acc = nullptr, *scratch_bonus = nullptr;
-  CUtensorMap tm_xn[4], tm_attn[4], tm_act[4];
+  CUtensorMap tm_xn[kNumBM], tm_attn[kNumBM], tm_act[kNumBM];
+  int M_alloc = 0;  // rows of the activation buffers (>= 256 for the widest token tile)
   int last_rows = 0, last_launches = 0;
   // profiling: event pairs around projection / attention launches
   bool profiling = false;
@@ -253,6 +262,7 @@ spec_status forward(spec_model* m, int B, int W, const int32_t* seq_ids, const i
       EpiParams e = base;
       e.N = m->qkv_n;
       e.K = d;
+      e.rscale = Ly.rs_qkv;
       e.splits = splits_for(e.N, e.K);
       e.split_stride = (long long)M * e.N;
       e.ssq_in = m->ssq_a;
@@ -274,6 +284,7 @@ spec_status forward(spec_model* m, int B, int W, const int32_t* seq_ids, const i
       EpiParams e = base;
       e.N = d;
       e.K = m->q_dim;
+      e.rscale = Ly.rs_o;
       e.splits = splits_for(e.N, e.K);
       e.split_stride = (long long)M * e.N;
       e.ssq_in = nullptr;
@@ -288,6 +299,7 @@ spec_status forward(spec_model* m, int B, int W, const int32_t* seq_ids, const i
       EpiParams e = base;
       e.N = 2 * F;
       e.K = d;
+      e.rscale = Ly.rs_gu;
       e.splits = splits_for(e.N, e.K);
       e.split_stride = (long long)M * e.N;
       e.ssq_in = m->ssq_b;
@@ -299,6 +311,7 @@ spec_status forward(spec_model* m, int B, int W, const int32_t* seq_ids, const i
       EpiParams e = base;
       e.N = d;
       e.K = F;
+      e.rscale = Ly.rs_down;
       e.splits = splits_for(e.N, e.K);
       e.split_stride = (long long)M * e.N;
       e.ssq_in = nullptr;
@@ -314,6 +327,7 @@ spec_status forward(spec_model* m, int B, int W, const int32_t* seq_ids, const i
     EpiParams e = base;
     e.N = c.vocab;
     e.K = d;
+    e.rscale = m->rs_lm;
     e.splits = 1;
     e.split_stride = 0;
     e.ssq_in = m->ssq_a;
@@ -462,6 +476,7 @@ spec_status spec_model_create(const spec_config* cfg, spec_model** out) {
 
   ALLOC(m->embed, (size_t)V * d);
   ALLOC(m->lm_head, (size_t)V * d);
+  ALLOC(m->rs_lm, V);
   ALLOC(m->final_norm, d);
   m->layers.resize(c.n_layers);
   for (auto& Ly : m->layers) {
@@ -469,6 +484,10 @@ spec_status spec_model_create(const spec_config* cfg, spec_model** out) {
     ALLOC(Ly.wo, (size_t)d * m->q_dim);
     ALLOC(Ly.wgu, (size_t)2 * F * d);
     ALLOC(Ly.wdown, (size_t)d * F);
+    ALLOC(Ly.rs_qkv, m->qkv_n);
+    ALLOC(Ly.rs_o, d);
+    ALLOC(Ly.rs_gu, 2 * F);
+    ALLOC(Ly.rs_down, d);
     ALLOC(Ly.attn_norm, d);
     ALLOC(Ly.ffn_norm, d);
   }
@@ -480,11 +499,12 @@ spec_status spec_model_create(const spec_config* cfg, spec_model** out) {
   ALLOC(m->page_table, (size_t)c.max_batch * m->max_pages);
   ALLOC(m->free_bits, (size_t)(c.num_pages + 31) / 32);
   ALLOC(m->status, 1);
+  m->M_alloc = std::max(M_max, 256);
   ALLOC(m->resid, (size_t)M_max * d);
-  ALLOC(m->xn, (size_t)M_max * d);
+  ALLOC(m->xn, (size_t)m->M_alloc * d);
   ALLOC(m->qrot, (size_t)M_max * m->q_dim);
-  ALLOC(m->attn_out, (size_t)M_max * m->q_dim);
-  ALLOC(m->act, (size_t)M_max * F);
+  ALLOC(m->attn_out, (size_t)m->M_alloc * m->q_dim);
+  ALLOC(m->act, (size_t)m->M_alloc * F);
   m->part_elems = std::max<long long>((long long)M_max * std::max({m->qkv_n, 2 * F, d}),
                                       16LL * std::min(M_max, 64) * std::max({m->qkv_n, 2 * F, d}));
   ALLOC(m->part, m->part_elems);
@@ -540,10 +560,10 @@ spec_status spec_model_create(const spec_config* cfg, spec_model** out) {
     ok &= make_map(&Ly.tm_down, Ly.wdown, F, d, 64, 128);
   }
   ok &= make_map(&m->tm_lm, m->lm_head, d, V, 64, 128);
-  for (int i = 0; i < 4; ++i) {
-    ok &= make_map(&m->tm_xn[i], m->xn, d, M_max, 64, kBMs[i]);
-    ok &= make_map(&m->tm_attn[i], m->attn_out, m->q_dim, M_max, 64, kBMs[i]);
-    ok &= make_map(&m->tm_act[i], m->act, F, M_max, 64, kBMs[i]);
+  for (int i = 0; i < kNumBM; ++i) {
+    ok &= make_map(&m->tm_xn[i], m->xn, d, m->M_alloc, 64, kBMs[i]);
+    ok &= make_map(&m->tm_attn[i], m->attn_out, m->q_dim, m->M_alloc, 64, kBMs[i]);
+    ok &= make_map(&m->tm_act[i], m->act, F, m->M_alloc, 64, kBMs[i]);
   }
   const uint64_t kv_rows = (uint64_t)c.n_layers * c.num_pages * c.n_kv_heads * kPage;
   ok &= make_map(&m->tm_k, m->kpool, hd, kv_rows, 64, 64);
@@ -586,13 +606,20 @@ spec_status spec_model_set_weight(spec_model* m, spec_weight which, int32_t laye
     return SPEC_OK;
   };
   spec_model::Layer* Ly = per_layer ? &m->layers[layer] : nullptr;
+  // matrices: copy the bf16 rows into place, then re-encode them in place as fp16 x 2^e
+  auto encode = [&](void* base, int K, int n_rows, int block, int block_stride, int row0,
+                    float* rscale) -> spec_status {
+    CUDA_TRY(launch_encode_rows(static_cast<uint16_t*>(base), K, n_rows, block, block_stride, row0, rscale, st));
+    return SPEC_OK;
+  };
   switch (which) {
     case SPEC_W_EMBED:
       if (auto s = expect((long long)c.vocab * d)) return s;
       return copy(m->embed, (size_t)n_elems * 2);
     case SPEC_W_LM_HEAD:
       if (auto s = expect((long long)c.vocab * d)) return s;
-      return copy(m->lm_head, (size_t)n_elems * 2);
+      if (auto s = copy(m->lm_head, (size_t)n_elems * 2)) return s;
+      return encode(m->lm_head, d, c.vocab, c.vocab, 0, 0, m->rs_lm);
     case SPEC_W_FINAL_NORM:
       if (auto s = expect(d)) return s;
       return copy(m->final_norm, (size_t)d * 4);
@@ -604,27 +631,33 @@ spec_status spec_model_set_weight(spec_model* m, spec_weight which, int32_t laye
       return copy(Ly->ffn_norm, (size_t)d * 4);
     case SPEC_W_WQ:
       if (auto s = expect((long long)m->q_dim * d)) return s;
-      return copy(Ly->wqkv, (size_t)n_elems * 2);
+      if (auto s = copy(Ly->wqkv, (size_t)n_elems * 2)) return s;
+      return encode(Ly->wqkv, d, m->q_dim, m->q_dim, 0, 0, Ly->rs_qkv);
     case SPEC_W_WK:
       if (auto s = expect((long long)m->kv_dim * d)) return s;
-      return copy(Ly->wqkv + (size_t)m->q_dim * d, (size_t)n_elems * 2);
+      if (auto s = copy(Ly->wqkv + (size_t)m->q_dim * d, (size_t)n_elems * 2)) return s;
+      return encode(Ly->wqkv, d, m->kv_dim, m->kv_dim, 0, m->q_dim, Ly->rs_qkv);
     case SPEC_W_WV:
       if (auto s = expect((long long)m->kv_dim * d)) return s;
-      return copy(Ly->wqkv + (size_t)(m->q_dim + m->kv_dim) * d, (size_t)n_elems * 2);
+      if (auto s = copy(Ly->wqkv + (size_t)(m->q_dim + m->kv_dim) * d, (size_t)n_elems * 2)) return s;
+      return encode(Ly->wqkv, d, m->kv_dim, m->kv_dim, 0, m->q_dim + m->kv_dim, Ly->rs_qkv);
     case SPEC_W_WO:
       if (auto s = expect((long long)d * m->q_dim)) return s;
-      return copy(Ly->wo, (size_t)n_elems * 2);
+      if (auto s = copy(Ly->wo, (size_t)n_elems * 2)) return s;
+      return encode(Ly->wo, m->q_dim, d, d, 0, 0, Ly->rs_o);
     case SPEC_W_DOWN:
       if (auto s = expect((long long)d * F)) return s;
-      return copy(Ly->wdown, (size_t)n_elems * 2);
+      if (auto s = copy(Ly->wdown, (size_t)n_elems * 2)) return s;
+      return encode(Ly->wdown, F, d, d, 0, 0, Ly->rs_down);
     case SPEC_W_GATE:
     case SPEC_W_UP: {
       if (auto s = expect((long long)F * d)) return s;
       // 64-row blocks interleaved: block j of gate -> rows 128j..128j+63, of up -> 128j+64..128j+127
       const size_t blk = (size_t)64 * d * 2;
+      const int off = which == SPEC_W_UP ? 64 : 0;
       char* dst = reinterpret_cast<char*>(Ly->wgu) + (which == SPEC_W_UP ? blk : 0);
       CUDA_TRY(cudaMemcpy2DAsync(dst, 2 * blk, src, blk, blk, F / 64, cudaMemcpyDefault, st));
-      return SPEC_OK;
+      return encode(Ly->wgu, d, F, 64, 128, off, Ly->rs_gu);
     }
     default:
       return fail(SPEC_ERR_INVALID_ARG, "unknown weight kind %d", (int)which);

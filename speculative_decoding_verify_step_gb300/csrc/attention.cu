@@ -12,7 +12,7 @@
 // tree whose ancestors of j are 0..j (section 10.3: each tree node sees only
 // its ancestors).
 //
-// K/V pages (64 tokens x head_dim bf16 per kv head) are streamed by TMA with
+// K/V pages (64 tokens x head_dim fp16 per kv head) are streamed by TMA with
 // the 128-byte swizzle into a 3-stage mbarrier pipeline fed by one producer
 // warp; consumer warps (16 query rows each) run QK^T and PV on mma.sync with
 // an online softmax in fp32 (exp2 domain).  A sequence's pages are split over a
@@ -137,7 +137,7 @@ __global__ void __launch_bounds__((kMaxRowTiles + 1) * 32)
     for (int ks = 0; ks < HD / 16; ++ks) {
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const __nv_bfloat16* qr =
+        const act_t* qr =
             p.q + ((long long)(b * p.W + jrow[h]) * p.Hq + head[h]) * HD + ks * 16 + 2 * c;
         const uint32_t lo = valid[h] ? *reinterpret_cast<const uint32_t*>(qr) : 0u;
         const uint32_t hi = valid[h] ? *reinterpret_cast<const uint32_t*>(qr + 8) : 0u;
@@ -177,8 +177,8 @@ __global__ void __launch_bounds__((kMaxRowTiles + 1) * 32)
           const int d = ks * 16 + ((lane >> 3) & 1) * 8;
           uint32_t b0, b1, b2, b3;
           ldsm_x4(kbase + (d >> 6) * (kPage * 128) + swz128(key, d & 63), b0, b1, b2, b3);
-          mma_bf16_16816(sc[2 * tp], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
-          mma_bf16_16816(sc[2 * tp + 1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+          mma_f16_16816(sc[2 * tp], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+          mma_f16_16816(sc[2 * tp + 1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
         }
       }
       // mask + online softmax (exp2 domain)
@@ -231,21 +231,21 @@ __global__ void __launch_bounds__((kMaxRowTiles + 1) * 32)
         acc[t][2] *= alpha[1];
         acc[t][3] *= alpha[1];
       }
-      // O += P V: P from the score registers (bf16), V via transposed ldmatrix
+      // O += P V: P from the score registers (fp16), V via transposed ldmatrix
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
-        const uint32_t a0 = pack_bf16x2(sc[2 * kk][0], sc[2 * kk][1]);
-        const uint32_t a1 = pack_bf16x2(sc[2 * kk][2], sc[2 * kk][3]);
-        const uint32_t a2 = pack_bf16x2(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
-        const uint32_t a3 = pack_bf16x2(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
+        const uint32_t a0 = pack_f16x2(sc[2 * kk][0], sc[2 * kk][1]);
+        const uint32_t a1 = pack_f16x2(sc[2 * kk][2], sc[2 * kk][3]);
+        const uint32_t a2 = pack_f16x2(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
+        const uint32_t a3 = pack_f16x2(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
 #pragma unroll
         for (int dp = 0; dp < HD / 16; ++dp) {
           const int key = kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
           const int d = dp * 16 + ((lane >> 4) & 1) * 8;
           uint32_t b0, b1, b2, b3;
           ldsm_x4_trans(vbase + (d >> 6) * (kPage * 128) + swz128(key, d & 63), b0, b1, b2, b3);
-          mma_bf16_16816(acc[2 * dp], a0, a1, a2, a3, b0, b1);
-          mma_bf16_16816(acc[2 * dp + 1], a0, a1, a2, a3, b2, b3);
+          mma_f16_16816(acc[2 * dp], a0, a1, a2, a3, b0, b1);
+          mma_f16_16816(acc[2 * dp + 1], a0, a1, a2, a3, b2, b3);
         }
       }
       __syncwarp();
@@ -309,7 +309,7 @@ __global__ void __launch_bounds__((kMaxRowTiles + 1) * 32)
 #pragma unroll
       for (int s = 0; s < kAttnCluster; ++s) num += wts[lr * kAttnCluster + s] * o[s];
       const int j = r / grp, hq = kvh * grp + r % grp;
-      p.out[((long long)(b * p.W + j) * p.Hq + hq) * HD + d] = __float2bfloat16(num);
+      p.out[((long long)(b * p.W + j) * p.Hq + hq) * HD + d] = to_act(num);
     }
   }
   // keep this CTA's shared memory alive until every CTA has read it

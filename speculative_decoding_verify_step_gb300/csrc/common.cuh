@@ -4,6 +4,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -18,6 +19,14 @@ namespace spec {
 constexpr int kPage = 64;            // tokens per KV page
 constexpr int kMaxWidth = 16;        // rows per sequence per forward
 constexpr unsigned long long kWaitBudgetCycles = 4000000000ull;  // ~2 s at 2 GHz
+
+// Compute format of activations, the KV cache and the stored weights: fp16.  The
+// bf16 weights are re-encoded exactly as fp16 times a per-row power of two (the
+// projection epilogue multiplies the row back by 2^-e), which keeps the weight
+// values and their bytes while giving activations 11 significant bits instead
+// of 8; accumulation is fp32 throughout.
+using act_t = __half;
+SPEC_DEVICE_INLINE act_t to_act(float x) { return __float2half_rn(fminf(fmaxf(x, -65504.f), 65504.f)); }
 
 // ---------------------------------------------------------------- status word
 // First error wins; kernels that hit an error skip the offending accesses.
@@ -131,26 +140,90 @@ SPEC_DEVICE_INLINE void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1,
                : "r"(addr));
 }
 
-// D(16x8 fp32) += A(16x16 bf16, row) * B(16x8 bf16, col)
-SPEC_DEVICE_INLINE void mma_bf16_16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
-                                       uint32_t b1) {
+// D(16x8 fp32) += A(16x16 f16, row) * B(16x8 f16, col)
+SPEC_DEVICE_INLINE void mma_f16_16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                      uint32_t b1) {
   asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-SPEC_DEVICE_INLINE uint32_t pack_bf16x2(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+SPEC_DEVICE_INLINE uint32_t pack_f16x2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Byte offset of element (row, col) in a tile whose rows are 128 bytes (64 bf16)
+// Byte offset of element (row, col) in a tile whose rows are 128 bytes (64 halves)
 // stored with the TMA 128-byte swizzle: 16-byte chunk j of row r lives at chunk
 // j ^ (r % 8).  The tile base must be 1024-byte aligned.
 SPEC_DEVICE_INLINE uint32_t swz128(int row, int col_elem) {
   return static_cast<uint32_t>(row * 128 + ((((col_elem >> 3) ^ (row & 7)) & 7) << 4) + ((col_elem & 7) << 1));
+}
+
+// ------------------------------------------------------------------- tcgen05
+// Tensor memory: allocation is warp-wide; the TMEM address lands in shared memory.
+SPEC_DEVICE_INLINE void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+}
+SPEC_DEVICE_INLINE void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+SPEC_DEVICE_INLINE void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+SPEC_DEVICE_INLINE void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+SPEC_DEVICE_INLINE void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row core
+// groups 1024 bytes apart (the layout a TMA 128B-swizzled box of 64 16-bit columns
+// produces).  Start address, LBO (unused for this layout), SBO, descriptor
+// version 1, swizzle mode 2 (128B).
+SPEC_DEVICE_INLINE uint64_t sdesc_k_sw128(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)1u << 16;
+  d |= (uint64_t)(1024u >> 4) << 32;
+  d |= (uint64_t)1u << 46;
+  d |= (uint64_t)2u << 61;
+  return d;
+}
+
+// Instruction descriptor of kind::f16 with f16 A and B (format 0), fp32 D (format 1),
+// both K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
+SPEC_DEVICE_INLINE void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accum) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
+      : "memory");
+}
+
+// Arrive on `bar` when every MMA this thread issued so far has completed.
+SPEC_DEVICE_INLINE void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+// 32 lanes x 16 columns of fp32 from TMEM: thread i gets lane (row) base+i, columns c..c+15.
+SPEC_DEVICE_INLINE void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 // ------------------------------------------------------------ block reductions

@@ -3,6 +3,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -15,14 +16,15 @@ extern bool g_use_pdl;
 // Message for spec_last_error() (thread-local), for entry points outside api.cu.
 void record_error(const char* msg);
 
-// Fused-epilogue projection (gemm.cu).  Y = X W^T over M rows; W: [N, K] bf16
-// (tensor map box {64, 128}), X: [M_alloc, K] bf16 (box {64, BM}, BM in 8/16/32/64).
+// Fused-epilogue projection (gemm.cu).  Y = X W^T over M rows; W: [N, K] fp16 with
+// a per-row scale (tensor map box {64, 128}), X: [M_alloc, K] fp16 (box {64, BM}).
 // split-K partials land in `part` ([splits][M][N] fp32); the last split CTA of a
 // tile reduces them and applies the epilogue:
 enum { kEpiQKV = 0, kEpiSwiGLU = 1, kEpiResid = 2, kEpiLogits = 3 };
 struct EpiParams {
   int M, N, K;
   int kb_total, kb_per_split, splits;  // kb_* filled by the launcher
+  const float* rscale;                 // [N] 2^-e of each weight row's fp16 encoding
   float* part;
   long long split_stride;
   int* counters;                       // one per (m tile, n tile), zero between launches
@@ -36,16 +38,16 @@ struct EpiParams {
   const int32_t* row_slot;
   const float* rope_cos;
   const float* rope_sin;
-  __nv_bfloat16* q_out;
-  __nv_bfloat16* kpool;                // this layer's base
-  __nv_bfloat16* vpool;
+  __half* q_out;
+  __half* kpool;                       // this layer's base
+  __half* vpool;
   // kEpiSwiGLU
-  __nv_bfloat16* act;
+  __half* act;
   int ffn;
-  // kEpiResid: resid += y, xn = bf16(resid * g_next), ssq_out partial sums
+  // kEpiResid: resid += y, xn = fp16(resid * g_next), ssq_out partial sums
   float* resid;
   const float* g_next;
-  __nv_bfloat16* xn;
+  __half* xn;
   float* ssq_out;
   int d;
   // kEpiLogits: logits and per-128-column (max, sum exp((l-max)/T), argmax) of each row
@@ -64,14 +66,16 @@ cudaError_t launch_gemm_epi(int epi, const CUtensorMap* tmW, const CUtensorMap* 
 int choose_splits(int N, int K, int M, int BM, int sm_count, int max_splits);
 int choose_bm(int M);
 
-// --- elementwise (elementwise.cu): resid = E[tok]; xn = bf16(E[tok] * g); ssq partials
+// --- elementwise (elementwise.cu): resid = E[tok]; xn = fp16(E[tok] * g); ssq partials
 cudaError_t launch_embed(const int32_t* tok, int M, const __nv_bfloat16* embed, const float* gain, int d, int vocab,
-                         float* resid, __nv_bfloat16* xn, float* ssq_out, int ssq_stride, int* status,
-                         cudaStream_t st);
+                         float* resid, __half* xn, float* ssq_out, int ssq_stride, int* status, cudaStream_t st);
+// bf16 rows -> fp16 * 2^e rows, in place; rscale[row] = 2^-e
+cudaError_t launch_encode_rows(uint16_t* w, int K, int n_rows, int block, int block_stride, int row0, float* rscale,
+                               cudaStream_t st);
 
 // --- attention (attention.cu)
 struct AttnParams {
-  const __nv_bfloat16* q;      // [M, Hq*hd] rotated queries
+  const __half* q;             // [M, Hq*hd] rotated queries
   const int32_t* page_table;   // [max_batch, max_pages]
   const int32_t* seq_ids;      // [B]
   const int32_t* seq_start;    // [B] cached length L at round start
@@ -80,7 +84,7 @@ struct AttnParams {
   int layer_row0;              // first TMA row of this layer in the KV pool maps
   int pages_per_split;         // pages per CTA; the cluster of kAttnCluster CTAs covers a sequence
   uint32_t anc[16];            // ancestor masks of the window rows (bit i: row i visible)
-  __nv_bfloat16* out;          // [M, Hq*hd]
+  __half* out;                 // [M, Hq*hd]
   int* status;
 };
 constexpr int kAttnCluster = 8;
@@ -176,8 +180,8 @@ struct TreeParams {
   int32_t* page_table;
   uint32_t* free_bits;
   int max_pages, max_batch;
-  __nv_bfloat16* kpool;
-  __nv_bfloat16* vpool;
+  __half* kpool;
+  __half* vpool;
   int n_layers, num_pages, Hkv, hd;
   int* status;
 };
@@ -198,7 +202,7 @@ cudaError_t launch_commit_all(const int32_t* seq_ids, int B, int W, int max_batc
 cudaError_t launch_alloc_to_len(const int32_t* seq_ids, const int32_t* lens, int n, int relative, int32_t* seq_len,
                                 int32_t* seq_npages, int32_t* page_table, uint32_t* free_bits, int max_pages,
                                 int num_pages, int max_batch, int* status, cudaStream_t st);
-cudaError_t launch_kv_fill_pages(__nv_bfloat16* kpool, __nv_bfloat16* vpool, const int32_t* page_table,
+cudaError_t launch_kv_fill_pages(__half* kpool, __half* vpool, const int32_t* page_table,
                                  const int32_t* seq_npages, int max_pages, const int32_t* seq_ids, int n,
                                  int n_layers, int num_pages, int Hkv, int hd, uint64_t seed, float scale,
                                  cudaStream_t st);

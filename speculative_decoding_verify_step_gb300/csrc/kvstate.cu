@@ -103,7 +103,7 @@ SPEC_DEVICE_INLINE uint64_t splitmix64(uint64_t x) {
 
 // Fill K and V of every allocated page of the listed sequences, all layers.
 // grid: (pages, n_layers, n); each block writes one (layer, page) of one sequence.
-__global__ void kv_fill_kernel(__nv_bfloat16* kpool, __nv_bfloat16* vpool, const int32_t* page_table,
+__global__ void kv_fill_kernel(act_t* kpool, act_t* vpool, const int32_t* page_table,
                                const int32_t* seq_npages, int max_pages, const int32_t* seq_ids, int num_pages,
                                int Hkv, int hd, uint64_t seed, float scale) {
   pdl_wait();
@@ -120,8 +120,8 @@ __global__ void kv_fill_kernel(__nv_bfloat16* kpool, __nv_bfloat16* vpool, const
     const uint64_t h = splitmix64(seed ^ (uint64_t)(base + e) * 0x2545F4914F6CDD1Dull);
     const float a = ((float)(uint32_t)(h & 0xffffffu) * (1.0f / 16777216.0f) * 2.f - 1.f) * scale;
     const float c = ((float)(uint32_t)((h >> 32) & 0xffffffu) * (1.0f / 16777216.0f) * 2.f - 1.f) * scale;
-    kpool[base + e] = __float2bfloat16(a);
-    vpool[base + e] = __float2bfloat16(c);
+    kpool[base + e] = to_act(a);
+    vpool[base + e] = to_act(c);
   }
 }
 
@@ -189,7 +189,7 @@ cudaError_t launch_alloc_to_len(const int32_t* seq_ids, const int32_t* lens, int
                   page_table, free_bits, max_pages, num_pages, max_batch, status);
 }
 
-cudaError_t launch_kv_fill_pages(__nv_bfloat16* kpool, __nv_bfloat16* vpool, const int32_t* page_table,
+cudaError_t launch_kv_fill_pages(act_t* kpool, act_t* vpool, const int32_t* page_table,
                                  const int32_t* seq_npages, int max_pages, const int32_t* seq_ids, int n,
                                  int n_layers, int num_pages, int Hkv, int hd, uint64_t seed, float scale,
                                  cudaStream_t st) {

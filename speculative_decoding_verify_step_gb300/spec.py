@@ -234,7 +234,7 @@ class SpecModel:
         v = torch.empty((n, Hkv, hd), dtype=torch.int16)
         _check(_lib.spec_read_kv(self.handle, layer, seq_id, t0, n, ctypes.c_void_p(k.data_ptr()),
                                  ctypes.c_void_p(v.data_ptr())))
-        return k.view(torch.bfloat16), v.view(torch.bfloat16)
+        return k.view(torch.float16), v.view(torch.float16)
 
     def debug_logits(self, rows: int) -> torch.Tensor:
         """Logits of the last forward ([rows, vocab] fp32, device)."""

@@ -1,0 +1,159 @@
+"""GPU parity at the Llama-3.1-8B widths (d 4096, 32/8 heads of 128, ffn 14336,
+vocab 128256).  A 2-layer model is compared with the oracle element by element at
+row counts that take both projection paths (<= 64 rows: mma.sync; 96 and 208
+rows: tcgen05); the full 32-layer model, in the launch configuration the bench
+times (B = 1, 1024 cached tokens), is checked through properties that hold at any
+size and through the oracle's page allocator."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import accept as A
+from oracle.decoder import PagedKV
+from speculative_decoding_verify_step_gb300 import synth
+from tests._gpu import cuda_model, need_gpu, oracle_for, rel_err, top2_gap
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-2
+
+
+@pytest.fixture(scope="module")
+def two_layer():
+    need_gpu()
+    dims = synth.LLAMA8B.with_layers(2)
+    w = {k: v.cpu() for k, v in synth.iter_weights(dims, seed=3, device="cuda", gain_jitter=0.1)}
+    kw = dict(max_batch=16, max_width=16, max_seq_len=256, num_pages=80)
+    m = cuda_model(dims, w, **kw)
+    o = oracle_for(dims, w, **kw)
+    yield dims, w, m, o
+    m.close()
+
+
+def _prefill_both(dims, m, o, lens, seed):
+    g = np.random.default_rng(seed)
+    prompts = [g.integers(0, dims.vocab, n) for n in lens]
+    ids = list(range(len(lens)))
+    m.seq_reset(list(range(16)))
+    o.reset(list(range(16)))
+    tok = torch.zeros(len(lens), max(lens), dtype=torch.int32)
+    for b, p in enumerate(prompts):
+        tok[b, :len(p)] = torch.as_tensor(p)
+    m.prefill(ids, tok.cuda(), list(lens))
+    o.prefill(ids, prompts)
+    return ids, prompts
+
+
+@pytest.mark.parametrize("B,W", [(1, 1), (1, 5), (1, 8), (1, 16), (4, 16), (8, 12), (16, 13)])
+def test_logits_match_oracle(two_layer, B, W):
+    dims, w, m, o = two_layer
+    lens = [70 + 7 * b for b in range(B)]              # ragged, across a page boundary
+    ids, prompts = _prefill_both(dims, m, o, lens, seed=B * 100 + W)
+    lm, pt = m.kv_state(ids)
+    assert lm == o.lengths(ids).tolist()
+    np.testing.assert_array_equal(np.array(pt), o.kv.page_table_array(ids))
+    g = np.random.default_rng(W)
+    tok = np.concatenate([np.array([[p[-1]] for p in prompts]), g.integers(0, dims.vocab, (B, W - 1))], axis=1)
+    got = m.score(ids, torch.from_numpy(tok).cuda()).cpu().numpy()
+    ref = o.forward(ids, tok)
+    assert rel_err(got, ref) < TOL, (B, W, rel_err(got, ref))
+    # K/V written by the window, layer 1, first sequence
+    n = lens[0] - 1 + W
+    k, v = m.read_kv(1, 0, 0, n)
+    kr = np.stack([o.kv.k[1, o.kv.slot(0, t)[0], :, o.kv.slot(0, t)[1]] for t in range(n)])
+    assert rel_err(k.float().numpy(), kr) < TOL
+
+
+def test_greedy_verify_rounds_match_oracle(two_layer):
+    dims, w, m, o = two_layer
+    ids, prompts = _prefill_both(dims, m, o, [80, 66, 90, 71], seed=7)
+    gamma = 4
+    hist = [list(map(int, p)) for p in prompts]
+    compared = 0
+    for r in range(3):
+        tok = np.zeros((4, gamma + 1), np.int64)
+        tok[:, 0] = [h[-1] for h in hist]
+        for i in range(1, gamma + 1):                 # drafts = the oracle's greedy continuation
+            tok[:, i] = o.forward(ids, tok[:, :i])[:, i - 1].argmax(-1)
+        tok[r % 4, 1 + r] = (tok[r % 4, 1 + r] + 1) % dims.vocab   # one wrong draft per round
+        ref = o.forward(ids, tok)
+        n_ref, com_ref, _ = A.accept_greedy(ref, tok[:, 1:])
+        acc, com, _ = m.verify_step(ids, torch.from_numpy(tok).cuda())
+        acc, com = acc.cpu().numpy(), com.cpu().numpy()
+        gap = top2_gap(ref)
+        for b in range(4):
+            if (gap[b, :n_ref[b] + 1] > 1e-2).all():
+                compared += 1
+                assert acc[b] == n_ref[b] and (com[b] == com_ref[b]).all()
+        o.commit(ids, n_ref, gamma + 1)
+        if not ((acc == n_ref).all() and (com == com_ref).all()):
+            break
+        for b in range(4):
+            hist[b].extend(int(t) for t in com_ref[b, :n_ref[b] + 1])
+        lens, pt = m.kv_state(ids)
+        assert lens == o.lengths(ids).tolist()
+        np.testing.assert_array_equal(np.array(pt), o.kv.page_table_array(ids))
+    assert compared >= 4
+
+
+@pytest.fixture(scope="module")
+def full_depth():
+    need_gpu()
+    dims = synth.LLAMA8B
+    m = cuda_model(dims, {}, max_batch=2, max_width=16, max_seq_len=2048, num_pages=70)
+    m.load_weights(synth.iter_weights(dims, seed=1, device="cuda"))
+    yield dims, m
+    m.close()
+
+
+def test_full_depth_window_equals_sequential_decode(full_depth):
+    """32 layers, 1024 cached tokens: one verify window of 8 rows scores what 8
+    decode steps score (prefix consistency), and its greedy decisions equal the
+    decode steps' tokens wherever the margin is clear."""
+    dims, m = full_depth
+    g = np.random.default_rng(5)
+    prompt = torch.from_numpy(g.integers(0, dims.vocab, (1, 1025))).int().cuda()
+    m.seq_reset([0])
+    m.prefill([0], prompt, [1025])
+    W = 8
+    win = torch.cat([prompt[:, -1:], torch.from_numpy(g.integers(0, dims.vocab, (1, W - 1))).int().cuda()], 1)
+    lw = m.score([0], win).cpu().numpy()[0]
+    m.seq_reset([0])
+    m.prefill([0], prompt, [1025])
+    seq = []
+    for j in range(W):                               # teacher-forced decode steps over the window
+        m.decode_step([0], win[:, j])
+        seq.append(m.debug_logits(1).cpu().numpy()[0])
+    m.sync_status()
+    seq = np.stack(seq)
+    assert rel_err(lw, seq) < TOL
+    gap = top2_gap(seq)
+    clear = gap > 1e-2
+    assert (lw.argmax(-1)[clear] == seq.argmax(-1)[clear]).all()
+
+
+def test_full_depth_page_tables_follow_the_oracle_allocator(full_depth):
+    """Page tables of two sequences through a prefill and several verify rounds equal
+    those the oracle's allocator produces from the same length history."""
+    dims, m = full_depth
+    g = np.random.default_rng(6)
+    lens0 = [1025, 700]
+    m.seq_reset([0, 1])
+    tok = torch.from_numpy(g.integers(0, dims.vocab, (2, 1025))).int().cuda()
+    m.prefill([0, 1], tok, lens0)
+    kv = PagedKV(1, 70, 1, 1, 2, m.max_pages)
+    for s, n in enumerate(lens0):                    # prefill reserves in sequence order
+        kv.ensure(s, n - 1)
+        kv.truncate(s, n - 1)
+    for r in range(6):
+        W = [5, 8, 3, 16, 2, 7][r]
+        t = torch.from_numpy(g.integers(0, dims.vocab, (2, W))).int().cuda()
+        acc, com, bon = m.verify_step([0, 1], t)
+        acc = acc.cpu().numpy()
+        for s in range(2):                           # the round reserves in batch order
+            kv.ensure(s, kv.length[s] + W)
+        for s in range(2):
+            kv.truncate(s, kv.length[s] + 1 + int(acc[s]))
+        lens, pt = m.kv_state([0, 1])
+        assert lens == kv.length
+        np.testing.assert_array_equal(np.array(pt), kv.page_table_array([0, 1]))
+    m.sync_status()
