@@ -43,7 +43,7 @@ struct AttnCfg {
   static constexpr int kSmemBytes = kAttnStages * kStageBytes + 2 * kAttnStages * 8 + 1024;
 };
 
-template <int HD>
+template <int HD, int CS>
 __global__ void __launch_bounds__((kMaxRowTiles + 1) * 32)
     attention_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                      const __grid_constant__ AttnParams p) {
@@ -64,15 +64,19 @@ __global__ void __launch_bounds__((kMaxRowTiles + 1) * 32)
   const int grp = p.Hq / p.Hkv;
   const int rows = p.W * grp;
 
-  pdl_wait();
+  // Sequence state and the cached pages were written by kernels that completed
+  // before the QKV projection (this kernel's predecessor) passed its own
+  // griddepcontrol.wait, which it does before letting this kernel launch; only
+  // q and the window's K/V come from the predecessor itself.  The successor (the
+  // O projection) only prefetches weights before its own wait, so it may launch
+  // right away.
   pdl_launch_dependents();
-
   const int sid = p.seq_ids[b];
   const bool sid_ok = sid >= 0 && sid < p.max_batch;  // a bad id was flagged by the prepare kernel
   const int L = p.seq_start[b];
   const int n_keys = L + p.W;
   const int n_pages = sid_ok ? min((n_keys + kPage - 1) / kPage, p.max_pages) : 0;
-  const int pps = (n_pages + kAttnCluster - 1) / kAttnCluster;
+  const int pps = (n_pages + CS - 1) / CS;
   const int pg0 = rank * pps;
   const int pg1 = min(pg0 + pps, n_pages);
   const int npg = max(0, pg1 - pg0);
@@ -98,9 +102,14 @@ __global__ void __launch_bounds__((kMaxRowTiles + 1) * 32)
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       const int32_t* pt = p.page_table + (long long)sid * p.max_pages;
+      bool waited = false;
       for (int i = 0; i < npg; ++i) {
         const int s = i % kAttnStages;
         const uint32_t use = i / kAttnStages;
+        if (!waited && (pg0 + i + 1) * kPage > L) {  // this page holds window slots
+          pdl_wait();
+          waited = true;
+        }
         if (i >= kAttnStages && !mbar_wait(&empty[s], (use - 1) & 1, p.status)) break;
         int page = pt[pg0 + i];
         if (page < 0) {  // no page: read page 0 instead (the round is already flagged)
@@ -120,6 +129,7 @@ __global__ void __launch_bounds__((kMaxRowTiles + 1) * 32)
     __syncwarp();
   } else {
     // ---------------------------------------------------------------- consumers
+    pdl_wait();  // q is written by the QKV projection
     const int g = lane >> 2, c = lane & 3;
     // query rows of this thread: r0 = warp*16 + g, r1 = r0 + 8; row r -> window row j = r / grp
     int jrow[2], head[2];
@@ -269,45 +279,46 @@ __global__ void __launch_bounds__((kMaxRowTiles + 1) * 32)
     }
   }
   // every CTA of the cluster has its partials in shared memory
+  if (warp == n_row_tiles) pdl_wait();  // every thread below may write the output
   cluster.sync();
   if (!s_fail) {
     // CTA `rank` merges rows rank, rank + 8, ...  First the per-row weights
     // w_s = 2^(m_s - max m) / sum_s 2^(m_s - max m) l_s (one pass over the 8 CTAs'
     // (m, l), kept in registers of the row's lane), then each output element is
     // sum_s w_s o_s[d] with the 8 remote loads independent of each other.
-    float* wts = part_l + kMaxRowTiles * 16;  // [8 rows][kAttnCluster] local scratch
-    const int n_my_rows = rows > rank ? (rows - rank + kAttnCluster - 1) / kAttnCluster : 0;
+    float* wts = part_l + kMaxRowTiles * 16;  // [rows per CTA][CS] local scratch
+    const int n_my_rows = rows > rank ? (rows - rank + CS - 1) / CS : 0;
     if (threadIdx.x < n_my_rows) {
-      const int r = rank + threadIdx.x * kAttnCluster;
-      float ms[kAttnCluster], ls[kAttnCluster];
+      const int r = rank + threadIdx.x * CS;
+      float ms[CS], ls[CS];
       float mmax = -INFINITY;
 #pragma unroll
-      for (int s = 0; s < kAttnCluster; ++s) {
+      for (int s = 0; s < CS; ++s) {
         ms[s] = cluster.map_shared_rank(part_m, s)[r];
         ls[s] = cluster.map_shared_rank(part_l, s)[r];
         mmax = fmaxf(mmax, ms[s]);
       }
       float den = 0.f;
 #pragma unroll
-      for (int s = 0; s < kAttnCluster; ++s) {
+      for (int s = 0; s < CS; ++s) {
         ms[s] = (mmax == -INFINITY || ms[s] == -INFINITY) ? 0.f : exp2f(ms[s] - mmax);
         den += ms[s] * ls[s];
       }
       const float inv = den > 0.f ? 1.f / den : 0.f;
 #pragma unroll
-      for (int s = 0; s < kAttnCluster; ++s) wts[threadIdx.x * kAttnCluster + s] = ms[s] * inv;
+      for (int s = 0; s < CS; ++s) wts[threadIdx.x * CS + s] = ms[s] * inv;
     }
     __syncthreads();
     for (int e = threadIdx.x; e < n_my_rows * HD; e += blockDim.x) {
       const int lr = e / HD;
-      const int r = rank + lr * kAttnCluster;
+      const int r = rank + lr * CS;
       const int d = e % HD;
-      float o[kAttnCluster];
+      float o[CS];
 #pragma unroll
-      for (int s = 0; s < kAttnCluster; ++s) o[s] = cluster.map_shared_rank(part_o, s)[r * HD + d];
+      for (int s = 0; s < CS; ++s) o[s] = cluster.map_shared_rank(part_o, s)[r * HD + d];
       float num = 0.f;
 #pragma unroll
-      for (int s = 0; s < kAttnCluster; ++s) num += wts[lr * kAttnCluster + s] * o[s];
+      for (int s = 0; s < CS; ++s) num += wts[lr * CS + s] * o[s];
       const int j = r / grp, hq = kvh * grp + r % grp;
       p.out[((long long)(b * p.W + j) * p.Hq + hq) * HD + d] = to_act(num);
     }
@@ -316,30 +327,36 @@ __global__ void __launch_bounds__((kMaxRowTiles + 1) * 32)
   cluster.sync();
 }
 
-template <int HD>
+template <int HD, int CS>
 cudaError_t launch_attention_hd(const CUtensorMap* tmK, const CUtensorMap* tmV, const AttnParams& p,
                                 cudaStream_t st) {
   using C = AttnCfg<HD>;
   static bool configured = false;
   if (!configured) {
     cudaError_t e =
-        cudaFuncSetAttribute(attention_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+        cudaFuncSetAttribute(attention_kernel<HD, CS>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e == cudaSuccess && CS > 8)
+      e = cudaFuncSetAttribute(attention_kernel<HD, CS>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
     configured = true;
   }
   const int rows = p.W * (p.Hq / p.Hkv);
   const int row_tiles = (rows + 15) / 16;
   if (row_tiles > kMaxRowTiles) return cudaErrorInvalidValue;
-  dim3 grid(kAttnCluster, p.Hkv, p.B);
-  return launch_k_cluster(attention_kernel<HD>, grid, dim3((row_tiles + 1) * 32), C::kSmemBytes, st,
-                          dim3(kAttnCluster, 1, 1), *tmK, *tmV, p);
+  dim3 grid(CS, p.Hkv, p.B);
+  return launch_k_cluster(attention_kernel<HD, CS>, grid, dim3((row_tiles + 1) * 32), C::kSmemBytes, st,
+                          dim3(CS, 1, 1), *tmK, *tmV, p);
 }
 
 }  // namespace
 
 cudaError_t launch_attention(const CUtensorMap* tmK, const CUtensorMap* tmV, const AttnParams& p, cudaStream_t st) {
-  if (p.hd == 128) return launch_attention_hd<128>(tmK, tmV, p, st);
-  if (p.hd == 64) return launch_attention_hd<64>(tmK, tmV, p, st);
+  // 16-CTA clusters while they still fit in one wave (two CTAs per SM), else 8
+  const bool wide = p.B * p.Hkv * 16 <= 2 * p.sm_count;
+  if (p.hd == 128) return wide ? launch_attention_hd<128, 16>(tmK, tmV, p, st)
+                               : launch_attention_hd<128, 8>(tmK, tmV, p, st);
+  if (p.hd == 64) return wide ? launch_attention_hd<64, 16>(tmK, tmV, p, st)
+                              : launch_attention_hd<64, 8>(tmK, tmV, p, st);
   return cudaErrorInvalidValue;
 }
 

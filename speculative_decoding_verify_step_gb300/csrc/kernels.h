@@ -82,12 +82,11 @@ struct AttnParams {
   int max_pages, max_batch;
   int B, W, Hq, Hkv, hd;
   int layer_row0;              // first TMA row of this layer in the KV pool maps
-  int pages_per_split;         // pages per CTA; the cluster of kAttnCluster CTAs covers a sequence
+  int sm_count;                // picks the cluster size (8 or 16 CTAs per sequence and kv head)
   uint32_t anc[16];            // ancestor masks of the window rows (bit i: row i visible)
   __half* out;                 // [M, Hq*hd]
   int* status;
 };
-constexpr int kAttnCluster = 8;
 cudaError_t launch_attention(const CUtensorMap* tmK, const CUtensorMap* tmV, const AttnParams& p, cudaStream_t st);
 
 // --- sequence state, acceptance and commit (accept.cu)
