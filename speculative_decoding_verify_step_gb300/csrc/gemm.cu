@@ -113,16 +113,20 @@ SPEC_DEVICE_INLINE void finish_tile(const EpiParams& p, float* tile, float* s_sc
   // weight-row scale 2^-e of the fp16 encoding, per output column of the tile
   __shared__ float s_rs[kBN];
   for (int cl = tid; cl < kBN; cl += NT) s_rs[cl] = p.rscale[n0 + cl];
-  // per-row scale of a normalised input: s_m = rsqrt(sum_t ssq[t][m] / d + eps)
-  for (int r = tid; r < ROWS; r += NT) {
-    float sc = 1.f;
+  // per-row scale of a normalised input: s_m = rsqrt(sum_t ssq[t][m] / d + eps).
+  // One warp per row, one tile partial per lane (independent loads, then a fixed
+  // shuffle tree: the same order on every run).
+#pragma unroll 4
+  for (int r = warp; r < ROWS; r += kGroupWarps) {
     const int m = m0 + r;
+    float sc = 1.f;
     if (p.ssq_in && m < p.M) {
       float ss = 0.f;
-      for (int t = 0; t < p.ssq_tiles; ++t) ss += __ldcg(p.ssq_in + (long long)t * p.ssq_stride + m);
+      for (int t = lane; t < p.ssq_tiles; t += 32) ss += __ldcg(p.ssq_in + (long long)t * p.ssq_stride + m);
+      ss = warp_sum(ss);
       sc = rsqrtf(ss * p.inv_d + p.eps);
     }
-    s_scale[r] = sc;
+    if (lane == 0) s_scale[r] = sc;
   }
   named_sync<NT>();
 
