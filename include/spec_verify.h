@@ -135,6 +135,26 @@ spec_status spec_verify_step(spec_model* m, int32_t B, int32_t gamma, const int3
                              const int32_t* tok, const float* q, const float* u, float temperature,
                              int32_t* accepted, int32_t* committed, int32_t* bonus, void* stream);
 
+/* Ragged verify: each sequence verifies its own number of rows, verify_lens[b]
+ * in [1, gamma+1] ("投机解码的性能收支" section 四: per-request verify lengths from
+ * a planner, modes static / cap-accept / compact; the planner itself needs a
+ * trained confidence head and is not here).  Sequence b accepts at most
+ * verify_lens[b] - 1 drafts; u[b, verify_lens[b]-1] drives its final draw.
+ *   mode SPEC_RAGGED_CAP_ACCEPT: the forward still scores gamma+1 rows per
+ *     sequence (tok [B, gamma+1]); only acceptance is capped.
+ *   mode SPEC_RAGGED_COMPACT: the forward scores only the real rows: tok is
+ *     packed, sequence b's rows after those of sequences < b (total_rows =
+ *     sum of verify_lens, passed on the host so the launch can be sized; the
+ *     device checks the sum).
+ * verify_lens: device [B].  q [B, gamma, V], u [B, gamma+1], committed
+ * [B, gamma+1] are padded per sequence as in spec_verify_step.  Both modes
+ * commit L + 1 + n_b and free trailing pages. */
+enum { SPEC_RAGGED_CAP_ACCEPT = 1, SPEC_RAGGED_COMPACT = 2 };
+spec_status spec_verify_ragged(spec_model* m, int32_t B, int32_t gamma, const int32_t* seq_ids, const int32_t* tok,
+                               const int32_t* verify_lens, int32_t total_rows, int32_t mode, const float* q,
+                               const float* u, float temperature, int32_t* accepted, int32_t* committed,
+                               int32_t* bonus, void* stream);
+
 /* Greedy token-tree verify (Lecture 6 section 10.3).  tok [B, n_nodes], node 0 =
  * pending token; parent_host: HOST [n_nodes], parent[0] = -1 and
  * 0 <= parent[c] < c (BFS order).  One forward under the ancestor mask (node c

@@ -309,9 +309,13 @@ __global__ void __launch_bounds__(kAccThreads) accept_round_kernel(const __grid_
   pdl_wait();
   pdl_launch_dependents();
   const int b = blockIdx.y;
-  const int W = p.gamma + 1;
   const int V = p.V;
-  const long long row0 = (long long)b * W;
+  const int Wmax = p.gamma + 1;                  // stride of u and committed
+  const int Wfwd = p.seq_wlen[b];                // rows the forward scored for this sequence
+  const int W = p.cap ? max(1, min(p.cap[b], Wfwd)) : Wfwd;  // rows the acceptance may use
+  const int gamma = W - 1;
+  const long long row0 = p.seq_rowoff[b];
+  const long long urow = (long long)b * Wmax;
   const int warp = threadIdx.x >> 5;
 
   if (warp < W) merge_row_stats(p, row0 + warp, SAMPLED, &s_max[warp], &s_z[warp], &s_am[warp]);
@@ -324,7 +328,7 @@ __global__ void __launch_bounds__(kAccThreads) accept_round_kernel(const __grid_
 
   if (threadIdx.x == 0) {
     int n = 0;
-    for (int i = 1; i <= p.gamma; ++i) {
+    for (int i = 1; i <= gamma; ++i) {
       const int x = xdraft(i);
       bool acc;
       if (x < 0 || x >= V) {
@@ -332,7 +336,7 @@ __global__ void __launch_bounds__(kAccThreads) accept_round_kernel(const __grid_
         acc = false;
       } else if constexpr (SAMPLED) {
         const float qx = p.q[((long long)b * p.gamma + (i - 1)) * V + x];
-        acc = __fmul_rn(p.u[row0 + i - 1], qx) < prob(i - 1, x);
+        acc = __fmul_rn(p.u[urow + i - 1], qx) < prob(i - 1, x);
       } else {
         acc = x == s_am[i - 1];
       }
@@ -345,7 +349,7 @@ __global__ void __launch_bounds__(kAccThreads) accept_round_kernel(const __grid_
   const int n = s_n;
 
   auto finish = [&](int tok_final) {  // one thread of the whole cluster
-    for (int j = 0; j < W; ++j) p.committed[row0 + j] = j < n ? xdraft(j + 1) : (j == n ? tok_final : -1);
+    for (int j = 0; j < Wmax; ++j) p.committed[urow + j] = j < n ? xdraft(j + 1) : (j == n ? tok_final : -1);
     p.accepted[b] = n;
     p.bonus[b] = tok_final;
     if (p.seq_ids) {
@@ -363,14 +367,14 @@ __global__ void __launch_bounds__(kAccThreads) accept_round_kernel(const __grid_
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = (int)cluster.block_rank();
     const int csize = (int)cluster.num_blocks();
-    const bool rejected = n < p.gamma;
+    const bool rejected = n < gamma;
     const float* qn = rejected ? p.q + ((long long)b * p.gamma + n) * V : nullptr;
     // this CTA's vocabulary slice, then this thread's sub-slice
     const int slice = (V + csize - 1) / csize;
     const int s0 = min(V, rank * slice), s1 = min(V, s0 + slice);
     const int chunk = (s1 - s0 + kAccThreads - 1) / kAccThreads;
     const int v0 = min(s1, s0 + (int)threadIdx.x * chunk), v1 = min(s1, v0 + chunk);
-    const unsigned long long m = (unsigned long long)floorf(p.u[row0 + p.gamma] * 16777216.0f);
+    const unsigned long long m = (unsigned long long)floorf(p.u[urow + gamma] * 16777216.0f);
     unsigned long long* tot_remote[kMaxDrawCluster];
     for (int pass = 0; pass < 2; ++pass) {
       const bool use_resid = rejected && pass == 0;

@@ -121,6 +121,7 @@ struct spec_model {
   float *tstat_max = nullptr, *tstat_sum = nullptr;  // [V/128][M_max] LM-head tile statistics
   int32_t* tstat_arg = nullptr;
   int32_t *row_pos = nullptr, *row_slot = nullptr, *seq_start = nullptr;
+  int32_t *seq_wlen = nullptr, *seq_rowoff = nullptr;  // per-call window layout (prepare kernel)
   float *rope_cos = nullptr, *rope_sin = nullptr;
   int32_t *scratch_ids = nullptr, *scratch_ids2 = nullptr, *scratch_tok = nullptr, *scratch_lens = nullptr;
   int32_t *scratch_acc = nullptr, *scratch_bonus = nullptr;
@@ -190,9 +191,10 @@ cudaError_t profiled(spec_model* m, int cls, double bytes, cudaStream_t st, F&& 
 // anc[j]: rows visible to row j inside the window.  want_logits: run the LM head
 // (with per-tile softmax statistics at temperature 1/inv_temp when `sampled`).
 spec_status forward(spec_model* m, int B, int W, const int32_t* seq_ids, const int32_t* tok, const int* depth,
-                    const uint32_t* anc, bool want_logits, bool sampled, float inv_temp, cudaStream_t st) {
+                    const uint32_t* anc, bool want_logits, bool sampled, float inv_temp, cudaStream_t st,
+                    const int32_t* wlen = nullptr, int total_rows = -1) {
   const spec_config& c = m->cfg;
-  const int M = B * W;
+  const int M = wlen ? total_rows : B * W;  // flat rows (ragged: the caller's total)
   const int d = c.d_model, hd = c.head_dim;
   const int Hq = c.n_heads, Hkv = c.n_kv_heads, F = c.ffn_dim;
 
@@ -200,6 +202,10 @@ spec_status forward(spec_model* m, int B, int W, const int32_t* seq_ids, const i
   pp.seq_ids = seq_ids;
   pp.B = B;
   pp.W = W;
+  pp.wlen = wlen;
+  pp.total_rows = M;
+  pp.seq_wlen = m->seq_wlen;
+  pp.seq_rowoff = m->seq_rowoff;
   pp.seq_len = m->seq_len;
   pp.seq_npages = m->seq_npages;
   pp.page_table = m->page_table;
@@ -240,6 +246,8 @@ spec_status forward(spec_model* m, int B, int W, const int32_t* seq_ids, const i
   ap.page_table = m->page_table;
   ap.seq_ids = seq_ids;
   ap.seq_start = m->seq_start;
+  ap.seq_wlen = m->seq_wlen;
+  ap.seq_rowoff = m->seq_rowoff;
   ap.max_pages = m->max_pages;
   ap.max_batch = c.max_batch;
   ap.B = B;
@@ -350,6 +358,9 @@ RoundAcceptParams round_params(spec_model* m, int B, int gamma, const int32_t* s
   RoundAcceptParams r{};
   r.B = B;
   r.gamma = gamma;
+  r.seq_wlen = m->seq_wlen;
+  r.seq_rowoff = m->seq_rowoff;
+  r.cap = nullptr;
   r.V = m->cfg.vocab;
   r.inv_temp = inv_temp;
   r.logits = m->logits;
@@ -519,6 +530,8 @@ spec_status spec_model_create(const spec_config* cfg, spec_model** out) {
   ALLOC(m->row_pos, M_max);
   ALLOC(m->row_slot, M_max);
   ALLOC(m->seq_start, c.max_batch);
+  ALLOC(m->seq_wlen, c.max_batch);
+  ALLOC(m->seq_rowoff, c.max_batch);
   ALLOC(m->rope_cos, (size_t)c.max_seq_len * (hd / 2));
   ALLOC(m->rope_sin, (size_t)c.max_seq_len * (hd / 2));
   ALLOC(m->scratch_ids, c.max_batch);
@@ -802,6 +815,43 @@ spec_status spec_verify_step(spec_model* m, int32_t B, int32_t gamma, const int3
   const float inv_t = sampled ? 1.f / temperature : 1.f;
   if (auto s = forward(m, B, W, seq_ids, tok, depth, anc, true, sampled, inv_t, st)) return s;
   RoundAcceptParams rp = round_params(m, B, gamma, seq_ids, tok, q, u, inv_t, accepted, committed, bonus);
+  CUDA_TRY(launch_accept_round(rp, sampled, st));
+  bump_bounds(m, W);
+  m->last_launches = g_launch_count;
+  return SPEC_OK;
+}
+
+spec_status spec_verify_ragged(spec_model* m, int32_t B, int32_t gamma, const int32_t* seq_ids, const int32_t* tok,
+                               const int32_t* verify_lens, int32_t total_rows, int32_t mode, const float* q,
+                               const float* u, float temperature, int32_t* accepted, int32_t* committed,
+                               int32_t* bonus, void* stream) {
+  if (spec_status s = check_model(m)) return s;
+  if (gamma < 0) return fail(SPEC_ERR_INVALID_ARG, "gamma < 0");
+  const int W = gamma + 1;
+  if (spec_status s = check_batch(m, B, W)) return s;
+  if (!seq_ids || !tok || !verify_lens || !accepted || !committed || !bonus)
+    return fail(SPEC_ERR_INVALID_ARG, "NULL argument");
+  if (mode != SPEC_RAGGED_CAP_ACCEPT && mode != SPEC_RAGGED_COMPACT) return fail(SPEC_ERR_INVALID_ARG, "bad mode");
+  if (mode == SPEC_RAGGED_COMPACT && (total_rows < B || total_rows > B * W))
+    return fail(SPEC_ERR_INVALID_ARG, "total_rows %d outside [B, B*(gamma+1)]", total_rows);
+  if (!(temperature >= 0.f) || std::isinf(temperature)) return fail(SPEC_ERR_INVALID_ARG, "bad temperature");
+  const bool sampled = temperature > 0.f;
+  if (sampled && (!u || (gamma > 0 && !q)))
+    return fail(SPEC_ERR_INVALID_ARG, "sampled verify needs q and u (no greedy fallback)");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int depth[16];
+  uint32_t anc[16];
+  chain_masks(W, depth, anc);
+  g_launch_count = 0;
+  const float inv_t = sampled ? 1.f / temperature : 1.f;
+  if (mode == SPEC_RAGGED_COMPACT) {
+    if (auto s = forward(m, B, W, seq_ids, tok, depth, anc, true, sampled, inv_t, st, verify_lens, total_rows))
+      return s;
+  } else {
+    if (auto s = forward(m, B, W, seq_ids, tok, depth, anc, true, sampled, inv_t, st)) return s;
+  }
+  RoundAcceptParams rp = round_params(m, B, gamma, seq_ids, tok, q, u, inv_t, accepted, committed, bonus);
+  if (mode == SPEC_RAGGED_CAP_ACCEPT) rp.cap = verify_lens;
   CUDA_TRY(launch_accept_round(rp, sampled, st));
   bump_bounds(m, W);
   m->last_launches = g_launch_count;

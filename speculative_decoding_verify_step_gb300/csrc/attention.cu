@@ -62,7 +62,6 @@ __global__ void __launch_bounds__((kMaxRowTiles + 1) * 32)
   const int lane = threadIdx.x & 31;
   const int n_row_tiles = blockDim.x / 32 - 1;
   const int grp = p.Hq / p.Hkv;
-  const int rows = p.W * grp;
 
   // Sequence state and the cached pages were written by kernels that completed
   // before the QKV projection (this kernel's predecessor) passed its own
@@ -74,7 +73,10 @@ __global__ void __launch_bounds__((kMaxRowTiles + 1) * 32)
   const int sid = p.seq_ids[b];
   const bool sid_ok = sid >= 0 && sid < p.max_batch;  // a bad id was flagged by the prepare kernel
   const int L = p.seq_start[b];
-  const int n_keys = L + p.W;
+  const int Wb = p.seq_wlen[b];      // this sequence's window rows (<= p.W)
+  const int row0 = p.seq_rowoff[b];  // its first flat row
+  const int rows = Wb * grp;
+  const int n_keys = L + Wb;
   const int n_pages = sid_ok ? min((n_keys + kPage - 1) / kPage, p.max_pages) : 0;
   const int pps = (n_pages + CS - 1) / CS;
   const int pg0 = rank * pps;
@@ -148,7 +150,7 @@ __global__ void __launch_bounds__((kMaxRowTiles + 1) * 32)
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const act_t* qr =
-            p.q + ((long long)(b * p.W + jrow[h]) * p.Hq + head[h]) * HD + ks * 16 + 2 * c;
+            p.q + ((long long)(row0 + jrow[h]) * p.Hq + head[h]) * HD + ks * 16 + 2 * c;
         const uint32_t lo = valid[h] ? *reinterpret_cast<const uint32_t*>(qr) : 0u;
         const uint32_t hi = valid[h] ? *reinterpret_cast<const uint32_t*>(qr + 8) : 0u;
         qa[ks][h] = lo;       // a0a1 (row g) / a2a3 (row g+8)
@@ -320,7 +322,7 @@ __global__ void __launch_bounds__((kMaxRowTiles + 1) * 32)
 #pragma unroll
       for (int s = 0; s < CS; ++s) num += wts[lr * CS + s] * o[s];
       const int j = r / grp, hq = kvh * grp + r % grp;
-      p.out[((long long)(b * p.W + j) * p.Hq + hq) * HD + d] = to_act(num);
+      p.out[((long long)(row0 + j) * p.Hq + hq) * HD + d] = to_act(num);
     }
   }
   // keep this CTA's shared memory alive until every CTA has read it

@@ -79,8 +79,10 @@ struct AttnParams {
   const int32_t* page_table;   // [max_batch, max_pages]
   const int32_t* seq_ids;      // [B]
   const int32_t* seq_start;    // [B] cached length L at round start
+  const int32_t* seq_wlen;     // [B] window rows of sequence b
+  const int32_t* seq_rowoff;   // [B] first flat row of sequence b
   int max_pages, max_batch;
-  int B, W, Hq, Hkv, hd;
+  int B, W, Hq, Hkv, hd;       // W: the widest window of the call
   int layer_row0;              // first TMA row of this layer in the KV pool maps
   int sm_count;                // picks the cluster size (8 or 16 CTAs per sequence and kv head)
   uint32_t anc[16];            // ancestor masks of the window rows (bit i: row i visible)
@@ -92,7 +94,11 @@ cudaError_t launch_attention(const CUtensorMap* tmK, const CUtensorMap* tmV, con
 // --- sequence state, acceptance and commit (accept.cu)
 struct PrepareParams {
   const int32_t* seq_ids;   // [B]
-  int B, W;
+  int B, W;                 // W: rows of every sequence, or the widest when `wlen` is given
+  const int32_t* wlen;      // [B] rows per sequence (device), or null: W each
+  int total_rows;           // sum of the rows (checked on the device when wlen is given)
+  int32_t* seq_wlen;        // [B] out: rows of sequence b
+  int32_t* seq_rowoff;      // [B] out: first flat row of sequence b
   int32_t* seq_len;         // [max_batch]
   int32_t* seq_npages;      // [max_batch]
   int32_t* page_table;      // [max_batch, max_pages]
@@ -141,7 +147,10 @@ cudaError_t launch_accept_chain(const AcceptParams& p, bool sampled, PSource src
 constexpr int kDrawCluster = 8;
 constexpr int kMaxDrawCluster = 16;
 struct RoundAcceptParams {
-  int B, gamma, V;
+  int B, gamma, V;           // gamma: the widest window - 1 (stride of q, u, committed)
+  const int32_t* seq_wlen;   // [B] window rows of sequence b
+  const int32_t* seq_rowoff; // [B] first flat row of sequence b
+  const int32_t* cap;        // [B] acceptance cap (verify length) or null
   float inv_temp;
   const float* logits;       // [B*W, V]
   int n_tiles;               // V / 128
@@ -150,8 +159,8 @@ struct RoundAcceptParams {
   const int32_t* tstat_arg;
   int tstat_stride;
   const float* q;            // [B, gamma, V] (sampled)
-  const int32_t* tok;        // [B, W] window tokens
-  const float* u;            // [B, W] (sampled)
+  const int32_t* tok;        // [rows] window tokens, sequence b at seq_rowoff[b]
+  const float* u;            // [B, gamma+1] (sampled)
   int32_t* accepted;
   int32_t* committed;        // [B, W]
   int32_t* bonus;

@@ -10,13 +10,20 @@ namespace spec {
 namespace {
 
 // One warp.  Sequences are served in batch order b = 0..B-1 (deterministic page
-// assignment).  For each window row j: position L + depth[j] (RoPE), KV slot L + j.
+// assignment).  Sequence b owns flat rows rowoff_b .. rowoff_b + W_b - 1; for its
+// window row j: position L + depth[j] (RoPE), KV slot L + j.
 __global__ void __launch_bounds__(32) prepare_kernel(const __grid_constant__ PrepareParams p) {
   pdl_wait();
   pdl_launch_dependents();
   const int lane = threadIdx.x;
+  int off = 0;
   for (int b = 0; b < p.B; ++b) {
     const int s = p.seq_ids[b];
+    int Wb = p.wlen ? p.wlen[b] : p.W;
+    if (Wb < 1 || Wb > p.W || off + Wb > p.total_rows) {  // refused, keeps every index in bounds
+      if (lane == 0) set_status(p.status, SPEC_ERR_INVALID_ARG);
+      Wb = max(0, min(min(Wb, p.W), p.total_rows - off));
+    }
     const bool sid_ok = s >= 0 && s < p.max_batch;
     int L = 0;
     bool ok = sid_ok;
@@ -24,16 +31,20 @@ __global__ void __launch_bounds__(32) prepare_kernel(const __grid_constant__ Pre
       if (lane == 0) set_status(p.status, SPEC_ERR_INVALID_ARG);
     } else {
       L = p.seq_len[s];
-      if (L + p.W > p.max_seq_len) {
+      if (L + Wb > p.max_seq_len) {
         ok = false;
       } else {
-        ok = warp_ensure_pages(s, L + p.W, p.seq_npages, p.page_table, p.max_pages, p.free_bits, p.num_pages);
+        ok = warp_ensure_pages(s, L + Wb, p.seq_npages, p.page_table, p.max_pages, p.free_bits, p.num_pages);
       }
       if (!ok && lane == 0) set_status(p.status, SPEC_ERR_CAPACITY);
     }
-    if (lane == 0) p.seq_start[b] = L;
-    for (int j = lane; j < p.W; j += 32) {
-      const int m = b * p.W + j;
+    if (lane == 0) {
+      p.seq_start[b] = L;
+      p.seq_wlen[b] = Wb;
+      p.seq_rowoff[b] = off;
+    }
+    for (int j = lane; j < Wb; j += 32) {
+      const int m = off + j;
       p.row_pos[m] = min(L + p.depth[j], p.max_seq_len - 1);
       int slot = -1;
       if (ok) {
@@ -44,8 +55,10 @@ __global__ void __launch_bounds__(32) prepare_kernel(const __grid_constant__ Pre
       const int tk = p.tok[m];
       if (tk < 0 || tk >= p.vocab) set_status(p.status, SPEC_ERR_INVALID_ARG);
     }
+    off += Wb;
     __syncwarp();
   }
+  if (lane == 0 && off != p.total_rows) set_status(p.status, SPEC_ERR_INVALID_ARG);
 }
 
 __global__ void seq_reset_kernel(const int32_t* seq_ids, int n, int32_t* seq_len, int32_t* seq_npages,

@@ -42,7 +42,9 @@ EXPORTS = ["spec_model_create", "spec_model_destroy", "spec_model_set_weight", "
            "spec_decode_step", "spec_verify_step", "spec_verify_tree_step", "spec_score", "spec_accept_probs",
            "spec_accept_greedy", "spec_get_kv_state", "spec_read_kv", "spec_debug_logits", "spec_kv_fill_random",
            "spec_sync_status", "spec_max_pages_per_seq", "spec_last_launch_count", "spec_last_error",
-           "spec_set_profiling", "spec_read_profile", "spec_accept_greedy_noalloc"]
+           "spec_set_profiling", "spec_read_profile", "spec_accept_greedy_noalloc", "spec_verify_ragged"]
+
+RAGGED_CAP_ACCEPT, RAGGED_COMPACT = 1, 2
 
 PROFILE_CLASSES = ["qkv", "o", "gate_up", "down", "lm_head", "attention"]
 
@@ -68,6 +70,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "spec_decode_step": (I32, [P, I32, P, P, F32, P, P, P]),
         "spec_verify_step": (I32, [P, I32, I32, P, P, P, P, F32, P, P, P, P]),
         "spec_verify_tree_step": (I32, [P, I32, I32, P, P, P, P, P, P, P]),
+        "spec_verify_ragged": (I32, [P, I32, I32, P, P, P, I32, I32, P, P, F32, P, P, P, P]),
         "spec_score": (I32, [P, I32, I32, P, P, P, P, P]),
         "spec_accept_probs": (I32, [I32, I32, I32, P, P, P, P, P, P, P, P]),
         "spec_accept_greedy": (I32, [I32, I32, I32, P, P, P, P, P, P]),
@@ -191,6 +194,26 @@ class SpecModel:
         acc, com, bon = outs
         _check(_lib.spec_verify_step(self.handle, B, W - 1, _ptr(sid), _ptr(tk), _ptr(q), _ptr(u),
                                      float(temperature), _ptr(acc), _ptr(com), _ptr(bon), _stream()))
+        return acc, com, bon
+
+    def verify_ragged(self, seq_ids, tok, verify_lens, mode: int, q=None, u=None, temperature: float = 0.0,
+                      gamma: Optional[int] = None, outs=None):
+        """mode RAGGED_CAP_ACCEPT: tok [B, gamma+1]; RAGGED_COMPACT: tok packed [sum(verify_lens)].
+        verify_lens: per-sequence rows (list or tensor).  Returns (accepted, committed [B, gamma+1], bonus)."""
+        sid = _dev_i32(seq_ids, self.device)
+        tk = _dev_i32(tok, self.device)
+        lens = _dev_i32(verify_lens, self.device)
+        B = sid.numel()
+        if gamma is None:
+            gamma = tk.shape[1] - 1 if mode == RAGGED_CAP_ACCEPT else int(lens.max().item()) - 1
+        total = int(tk.numel()) if mode == RAGGED_COMPACT else B * (gamma + 1)
+        if outs is None:
+            outs = (torch.empty(B, dtype=torch.int32, device=self.device),
+                    torch.empty(B, gamma + 1, dtype=torch.int32, device=self.device),
+                    torch.empty(B, dtype=torch.int32, device=self.device))
+        acc, com, bon = outs
+        _check(_lib.spec_verify_ragged(self.handle, B, gamma, _ptr(sid), _ptr(tk), _ptr(lens), total, mode, _ptr(q),
+                                       _ptr(u), float(temperature), _ptr(acc), _ptr(com), _ptr(bon), _stream()))
         return acc, com, bon
 
     def verify_tree_step(self, seq_ids, tok, parent: Sequence[int], outs=None):
