@@ -30,6 +30,10 @@ Readings where the pages leave a step open (each is listed in the design doc):
 * The final draw is an integer inverse CDF (see `draw_index`) so that it is
   reproducible bit for bit under any summation order.
 * Greedy ties go to the lowest token index.
+* Sampling adjustments (`adjust_probs`): temperature first (in `target_probs`),
+  then top-k, then top-p over the top-k renormalised distribution; rank order is
+  p descending with the lower token index first on equal p; masses on the same
+  2^-40 grid as the final draw, so set membership is exact integer arithmetic.
 """
 from __future__ import annotations
 
@@ -50,6 +54,67 @@ def target_probs(logits: np.ndarray, temperature: float) -> np.ndarray:
     z = z - z.max(axis=-1, keepdims=True)
     e = np.exp(z)
     return (e / e.sum(axis=-1, keepdims=True)).astype(np.float32)
+
+
+# ---------------------------------------------------------- sampling adjustments
+def adjust_probs(p_row: np.ndarray, top_k: int, top_p: float) -> np.ndarray:
+    """Top-k then top-p (nucleus) renormalisation of one probability row.
+
+    Lecture 6 "Optimizing Autoregressive Decode" section 7.3: each sampling setting
+    is sampling from an adjusted distribution (top-k: every token ranked after the
+    k-th gets probability zero; top-p: the smallest set of top-ranked tokens whose
+    mass reaches p), and speculative sampling on the adjusted p and q follows the
+    adjusted p.  "Per-step cost versus accepted tokens", section "Reefs": the
+    renormalisation after top-k / top-p happens at verify time, for top_p < 1 or
+    top_k > 1.  Readings (the pages fix neither the order nor the arithmetic):
+
+    * rank order: p descending, lower token index first among equal p;
+    * top_k in [1, V) is active (0 or >= V: off); top_p in (0, 1) is active (1: off);
+    * masses R_v = floor(p_v * 2^40) (the final draw's grid); with the first k ranked
+      tokens (all V when top-k is off) of mass S_k, the nucleus is the shortest
+      ranked prefix (at least one token) whose mass reaches
+      ceil(fl64(top_p) * S_k) -- top-p acts on the top-k renormalised distribution;
+    * kept tokens get fl32(fl64(R_v) * fl64(1 / Z)), Z = their summed mass (a
+      float64 reciprocal, then one float64 product per token); all others 0.  With
+      no adjustment active, or Z = 0, p is returned unchanged.
+    """
+    p = np.asarray(p_row, dtype=np.float32)
+    V = p.size
+    k_on = 1 <= int(top_k) < V
+    p_on = float(np.float32(top_p)) < 1.0
+    if not (k_on or p_on):
+        return p.copy()
+    pk = np.where(p > 0, p, np.float32(0.0))
+    order = np.lexsort((np.arange(V), -pk.astype(np.float64)))   # last key is primary
+    R = [int(r) for r in fixed_point_mass(pk[order])]
+    n = int(top_k) if k_on else V
+    if p_on:
+        s_k = sum(R[:n])
+        tau = max(1, int(np.ceil(np.float64(np.float32(top_p)) * np.float64(s_k))))
+        run, n_p = 0, n
+        for i in range(n):
+            run += R[i]
+            if run >= tau:
+                n_p = i + 1
+                break
+        n = n_p
+    Z = sum(R[:n])
+    if Z == 0:
+        return p.copy()
+    out = np.zeros(V, dtype=np.float32)
+    inv = np.float64(1.0) / np.float64(Z)
+    out[order[:n]] = (np.array(R[:n], dtype=np.float64) * inv).astype(np.float32)
+    return out
+
+
+def adjust_rows(p: np.ndarray, top_k, top_p) -> np.ndarray:
+    """`adjust_probs` on every row of p [B, W, V]; top_k, top_p per sequence [B]."""
+    p = np.asarray(p, dtype=np.float32)
+    out = np.empty_like(p)
+    for b in range(p.shape[0]):
+        for j in range(p.shape[1]):
+            out[b, j] = adjust_probs(p[b, j], int(np.asarray(top_k)[b]), float(np.asarray(top_p)[b]))
+    return out
 
 
 # ------------------------------------------------------------------- greedy chain
