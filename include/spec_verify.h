@@ -116,24 +116,46 @@ spec_status spec_seq_reset(spec_model* m, int32_t n, const int32_t* seq_ids_host
 spec_status spec_prefill(spec_model* m, int32_t B, const int32_t* seq_ids, const int32_t* tokens,
                          int32_t stride, const int32_t* lens_host, void* stream);
 
+/* Sampling adjustments of sampled rounds (Lecture 6 "Optimizing Autoregressive
+ * Decode" section 7.3; "Per-step cost versus accepted tokens", section "Reefs"):
+ * top_k, top_p are device arrays [B] (either may be NULL = off for every
+ * sequence).  top_k[b] in [1, vocab) keeps sequence b's k most probable tokens
+ * (0 or >= vocab: off); top_p[b] in (0, 1) then keeps the shortest top-ranked
+ * prefix whose mass reaches top_p of the top-k renormalised mass (1: off).
+ * Rank order: p descending, lower token index first on equal p; masses on the
+ * 2^-40 grid, R_v = floor(p_v * 2^40), nucleus = the shortest prefix with summed R
+ * >= ceil(fl64(top_p) * S_k); kept tokens get fl32(fl64(R_v) * fl64(1/Z)), Z =
+ * their summed R.  The target p of every window row is adjusted before the
+ * accept tests, the residual and the bonus draw; q must be the draft
+ * distribution the drafts were drawn from -- adjusted the same way (see
+ * spec_adjust_probs) for the best acceptance, though any q keeps the output law
+ * equal to the adjusted p.  Ignored when temperature == 0 (the argmax is
+ * unchanged).  A setting outside its range sets SPEC_ERR_INVALID_ARG in the
+ * status word and leaves that sequence unadjusted.  Supported for vocab <=
+ * 393216 (SPEC_ERR_INVALID_ARG otherwise). */
+
 /* Baseline decode step (q_len = 1): one forward over the pending tokens tok[B],
  * then argmax (temperature == 0) or one draw from softmax(logits/T) with u[B]
- * (temperature > 0; u required).  Writes next_tok[B] and commits (L += 1). */
+ * (temperature > 0; u required), adjusted by top_k / top_p as above.  Writes
+ * next_tok[B] and commits (L += 1). */
 spec_status spec_decode_step(spec_model* m, int32_t B, const int32_t* seq_ids, const int32_t* tok,
-                             float temperature, const float* u, int32_t* next_tok, void* stream);
+                             float temperature, const int32_t* top_k, const float* top_p, const float* u,
+                             int32_t* next_tok, void* stream);
 
 /* Verify round.  tok [B, gamma+1]: pending token + gamma drafts.
  * temperature == 0: greedy, q and u must be NULL or are ignored.
  * temperature > 0: q [B, gamma, vocab] fp32 draft distributions (q[b, i-1] is
  * the distribution draft x_i was drawn from, over the same temperature-adjusted
  * vocabulary), u [B, gamma+1] fp32 uniforms in [0,1): u[b, i-1] drives the test
- * of x_i and u[b, gamma] the one final draw.
+ * of x_i and u[b, gamma] the one final draw.  top_k, top_p: sampling
+ * adjustments as above (NULL = off).
  * Outputs: accepted [B] = n_b; committed [B, gamma+1] = x_1..x_n then the
  * resampled or bonus token, -1 after; bonus [B] = that last token.
  * Commits L <- L + 1 + n_b and frees trailing pages.  1 <= gamma+1 <= max_width. */
 spec_status spec_verify_step(spec_model* m, int32_t B, int32_t gamma, const int32_t* seq_ids,
                              const int32_t* tok, const float* q, const float* u, float temperature,
-                             int32_t* accepted, int32_t* committed, int32_t* bonus, void* stream);
+                             const int32_t* top_k, const float* top_p, int32_t* accepted, int32_t* committed,
+                             int32_t* bonus, void* stream);
 
 /* Ragged verify: each sequence verifies its own number of rows, verify_lens[b]
  * in [1, gamma+1] ("投机解码的性能收支" section 四: per-request verify lengths from
@@ -147,13 +169,13 @@ spec_status spec_verify_step(spec_model* m, int32_t B, int32_t gamma, const int3
  *     sum of verify_lens, passed on the host so the launch can be sized; the
  *     device checks the sum).
  * verify_lens: device [B].  q [B, gamma, V], u [B, gamma+1], committed
- * [B, gamma+1] are padded per sequence as in spec_verify_step.  Both modes
- * commit L + 1 + n_b and free trailing pages. */
+ * [B, gamma+1] are padded per sequence as in spec_verify_step; top_k, top_p as
+ * there.  Both modes commit L + 1 + n_b and free trailing pages. */
 enum { SPEC_RAGGED_CAP_ACCEPT = 1, SPEC_RAGGED_COMPACT = 2 };
 spec_status spec_verify_ragged(spec_model* m, int32_t B, int32_t gamma, const int32_t* seq_ids, const int32_t* tok,
                                const int32_t* verify_lens, int32_t total_rows, int32_t mode, const float* q,
-                               const float* u, float temperature, int32_t* accepted, int32_t* committed,
-                               int32_t* bonus, void* stream);
+                               const float* u, float temperature, const int32_t* top_k, const float* top_p,
+                               int32_t* accepted, int32_t* committed, int32_t* bonus, void* stream);
 
 /* Greedy token-tree verify (Lecture 6 section 10.3).  tok [B, n_nodes], node 0 =
  * pending token; parent_host: HOST [n_nodes], parent[0] = -1 and
@@ -181,6 +203,17 @@ spec_status spec_score(spec_model* m, int32_t B, int32_t W, const int32_t* seq_i
 spec_status spec_accept_probs(int32_t B, int32_t gamma, int32_t V, const float* p, const float* q,
                               const int32_t* x, const float* u, int32_t* accepted, int32_t* committed,
                               int32_t* bonus, void* stream);
+
+/* Sampling adjustment of given probability rows (no model): p_out = top-k /
+ * top-p adjustment of p (definition above spec_decode_step), row r using setting
+ * r / rows_per_setting of top_k / top_p (device arrays; either may be NULL = off).
+ * p, p_out: device [rows, V] fp32 probabilities (entries in [0, 1]); p_out may
+ * equal p.  Rows whose setting is off, or outside its range (no status word
+ * here: the row is left as it is), are copied unchanged.  For adjusting the
+ * draft's q the same way as the target's p, and for spec_accept_probs on
+ * adjusted rows.  rows <= 65535, V <= 393216. */
+spec_status spec_adjust_probs(int32_t rows, int32_t V, const float* p, float* p_out, const int32_t* top_k,
+                              const float* top_p, int32_t rows_per_setting, void* stream);
 
 /* Standalone greedy acceptance on given logits [B, gamma+1, V] and drafts x [B, gamma]. */
 spec_status spec_accept_greedy(int32_t B, int32_t gamma, int32_t V, const float* logits, const int32_t* x,

@@ -27,6 +27,7 @@
 
 #include "kvstate.cuh"
 #include "launch.cuh"
+#include "sampling.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -320,9 +321,24 @@ __global__ void __launch_bounds__(kAccThreads) accept_round_kernel(const __grid_
 
   if (warp < W) merge_row_stats(p, row0 + warp, SAMPLED, &s_max[warp], &s_z[warp], &s_am[warp]);
   __syncthreads();
+  // top-k / top-p: the selection kernel's statistics and kept set of each row
+  __shared__ SelRow s_sel[kMaxWidth];
+  __shared__ double s_inv[kMaxWidth];
+  const bool adjust = SAMPLED && p.sel != nullptr;
+  if (adjust) {
+    if (threadIdx.x < W) {
+      const long long r = row0 + threadIdx.x;
+      s_max[threadIdx.x] = p.sel_max[r];
+      s_z[threadIdx.x] = p.sel_z[r];
+      s_sel[threadIdx.x] = p.sel[r];
+      s_inv[threadIdx.x] = sel_inv_z(s_sel[threadIdx.x]);
+    }
+    __syncthreads();
+  }
 
   auto prob = [&](int row, int v) -> float {
-    return expf((p.logits[(row0 + row) * V + v] - s_max[row]) * p.inv_temp) / s_z[row];
+    const float pv = prob_from_logit(p.logits[(row0 + row) * V + v], s_max[row], p.inv_temp, s_z[row]);
+    return adjust ? adjusted_prob(pv, v, s_sel[row], s_inv[row]) : pv;
   };
   auto xdraft = [&](int i) -> int { return p.tok[row0 + i]; };  // x_i = window row i
 

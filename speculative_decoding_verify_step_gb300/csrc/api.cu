@@ -12,6 +12,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "sampling.cuh"
 
 namespace spec {
 bool g_use_pdl = true;
@@ -120,6 +121,8 @@ struct spec_model {
   float* logits = nullptr;
   float *tstat_max = nullptr, *tstat_sum = nullptr;  // [V/128][M_max] LM-head tile statistics
   int32_t* tstat_arg = nullptr;
+  SelRow* sel = nullptr;                  // [M_max] top-k / top-p kept set of each window row
+  float *sel_max = nullptr, *sel_z = nullptr;
   int32_t *row_pos = nullptr, *row_slot = nullptr, *seq_start = nullptr;
   int32_t *seq_wlen = nullptr, *seq_rowoff = nullptr;  // per-call window layout (prepare kernel)
   float *rope_cos = nullptr, *rope_sin = nullptr;
@@ -383,7 +386,40 @@ RoundAcceptParams round_params(spec_model* m, int B, int gamma, const int32_t* s
   r.max_pages = m->max_pages;
   r.max_batch = m->cfg.max_batch;
   r.status = m->status;
+  r.sel = nullptr;
+  r.sel_max = nullptr;
+  r.sel_z = nullptr;
   return r;
+}
+
+// Top-k / top-p of a sampled round: one selection launch over every window row,
+// whose kept sets and softmax statistics the acceptance then uses.
+spec_status adjust_round(spec_model* m, int B, int Wmax, const int32_t* top_k, const float* top_p,
+                         RoundAcceptParams& rp, cudaStream_t st) {
+  if (!top_k && !top_p) return SPEC_OK;
+  if (m->cfg.vocab > select_max_vocab())
+    return fail(SPEC_ERR_INVALID_ARG, "top-k / top-p supports vocabularies up to %d", select_max_vocab());
+  SelectParams sp{};
+  sp.V = m->cfg.vocab;
+  sp.top_k = top_k;
+  sp.top_p = top_p;
+  sp.logits = m->logits;
+  sp.tstat_max = m->tstat_max;
+  sp.tstat_sum = m->tstat_sum;
+  sp.n_tiles = m->cfg.vocab / 128;
+  sp.tstat_stride = m->M_max;
+  sp.inv_temp = rp.inv_temp;
+  sp.seq_wlen = m->seq_wlen;
+  sp.seq_rowoff = m->seq_rowoff;
+  sp.sel = m->sel;
+  sp.row_max = m->sel_max;
+  sp.row_z = m->sel_z;
+  sp.status = m->status;
+  CUDA_TRY(launch_select(sp, PSource::kLogits, Wmax, B, st));
+  rp.sel = m->sel;
+  rp.sel_max = m->sel_max;
+  rp.sel_z = m->sel_z;
+  return SPEC_OK;
 }
 
 constexpr int kProfMax = 1024;
@@ -527,6 +563,9 @@ spec_status spec_model_create(const spec_config* cfg, spec_model** out) {
   ALLOC(m->tstat_max, (size_t)(V / 128) * M_max);
   ALLOC(m->tstat_sum, (size_t)(V / 128) * M_max);
   ALLOC(m->tstat_arg, (size_t)(V / 128) * M_max);
+  ALLOC(m->sel, M_max);
+  ALLOC(m->sel_max, M_max);
+  ALLOC(m->sel_z, M_max);
   ALLOC(m->row_pos, M_max);
   ALLOC(m->row_slot, M_max);
   ALLOC(m->seq_start, c.max_batch);
@@ -773,7 +812,8 @@ spec_status spec_score(spec_model* m, int32_t B, int32_t W, const int32_t* seq_i
 }
 
 spec_status spec_decode_step(spec_model* m, int32_t B, const int32_t* seq_ids, const int32_t* tok, float temperature,
-                             const float* u, int32_t* next_tok, void* stream) {
+                             const int32_t* top_k, const float* top_p, const float* u, int32_t* next_tok,
+                             void* stream) {
   if (spec_status s = check_model(m)) return s;
   if (spec_status s = check_batch(m, B, 1)) return s;
   if (!seq_ids || !tok || !next_tok) return fail(SPEC_ERR_INVALID_ARG, "NULL argument");
@@ -789,6 +829,8 @@ spec_status spec_decode_step(spec_model* m, int32_t B, const int32_t* seq_ids, c
   if (auto s = forward(m, B, 1, seq_ids, tok, depth, anc, true, sampled, inv_t, st)) return s;
   RoundAcceptParams rp = round_params(m, B, 0, seq_ids, tok, nullptr, u, inv_t, m->scratch_acc, next_tok,
                                       m->scratch_bonus);
+  if (sampled)
+    if (auto s = adjust_round(m, B, 1, top_k, top_p, rp, st)) return s;
   CUDA_TRY(launch_accept_round(rp, sampled, st));
   bump_bounds(m, 1);
   m->last_launches = g_launch_count;
@@ -796,8 +838,9 @@ spec_status spec_decode_step(spec_model* m, int32_t B, const int32_t* seq_ids, c
 }
 
 spec_status spec_verify_step(spec_model* m, int32_t B, int32_t gamma, const int32_t* seq_ids, const int32_t* tok,
-                             const float* q, const float* u, float temperature, int32_t* accepted, int32_t* committed,
-                             int32_t* bonus, void* stream) {
+                             const float* q, const float* u, float temperature, const int32_t* top_k,
+                             const float* top_p, int32_t* accepted, int32_t* committed, int32_t* bonus,
+                             void* stream) {
   if (spec_status s = check_model(m)) return s;
   if (gamma < 0) return fail(SPEC_ERR_INVALID_ARG, "gamma < 0");
   const int W = gamma + 1;
@@ -815,6 +858,8 @@ spec_status spec_verify_step(spec_model* m, int32_t B, int32_t gamma, const int3
   const float inv_t = sampled ? 1.f / temperature : 1.f;
   if (auto s = forward(m, B, W, seq_ids, tok, depth, anc, true, sampled, inv_t, st)) return s;
   RoundAcceptParams rp = round_params(m, B, gamma, seq_ids, tok, q, u, inv_t, accepted, committed, bonus);
+  if (sampled)
+    if (auto s = adjust_round(m, B, W, top_k, top_p, rp, st)) return s;
   CUDA_TRY(launch_accept_round(rp, sampled, st));
   bump_bounds(m, W);
   m->last_launches = g_launch_count;
@@ -823,8 +868,8 @@ spec_status spec_verify_step(spec_model* m, int32_t B, int32_t gamma, const int3
 
 spec_status spec_verify_ragged(spec_model* m, int32_t B, int32_t gamma, const int32_t* seq_ids, const int32_t* tok,
                                const int32_t* verify_lens, int32_t total_rows, int32_t mode, const float* q,
-                               const float* u, float temperature, int32_t* accepted, int32_t* committed,
-                               int32_t* bonus, void* stream) {
+                               const float* u, float temperature, const int32_t* top_k, const float* top_p,
+                               int32_t* accepted, int32_t* committed, int32_t* bonus, void* stream) {
   if (spec_status s = check_model(m)) return s;
   if (gamma < 0) return fail(SPEC_ERR_INVALID_ARG, "gamma < 0");
   const int W = gamma + 1;
@@ -852,6 +897,8 @@ spec_status spec_verify_ragged(spec_model* m, int32_t B, int32_t gamma, const in
   }
   RoundAcceptParams rp = round_params(m, B, gamma, seq_ids, tok, q, u, inv_t, accepted, committed, bonus);
   if (mode == SPEC_RAGGED_CAP_ACCEPT) rp.cap = verify_lens;
+  if (sampled)
+    if (auto s = adjust_round(m, B, W, top_k, top_p, rp, st)) return s;
   CUDA_TRY(launch_accept_round(rp, sampled, st));
   bump_bounds(m, W);
   m->last_launches = g_launch_count;
@@ -920,6 +967,25 @@ spec_status spec_accept_probs(int32_t B, int32_t gamma, int32_t V, const float* 
   ap.committed = committed;
   ap.bonus = bonus;
   CUDA_TRY(launch_accept_chain(ap, true, PSource::kProbs, static_cast<cudaStream_t>(stream)));
+  return SPEC_OK;
+}
+
+spec_status spec_adjust_probs(int32_t rows, int32_t V, const float* p, float* p_out, const int32_t* top_k,
+                              const float* top_p, int32_t rows_per_setting, void* stream) {
+  if (rows < 1 || V < 1 || rows_per_setting < 1) return fail(SPEC_ERR_INVALID_ARG, "bad shape");
+  if (rows > 65535) return fail(SPEC_ERR_INVALID_ARG, "at most 65535 rows per call");
+  if (V > select_max_vocab())
+    return fail(SPEC_ERR_INVALID_ARG, "top-k / top-p supports vocabularies up to %d", select_max_vocab());
+  if (!p || !p_out) return fail(SPEC_ERR_INVALID_ARG, "NULL argument");
+  SelectParams sp{};
+  sp.V = V;
+  sp.top_k = top_k;
+  sp.top_p = top_p;
+  sp.p_in = p;
+  sp.p_out = p_out;
+  sp.rows_per_set = rows_per_setting;
+  sp.status = nullptr;
+  CUDA_TRY(launch_select(sp, PSource::kProbs, rows, 1, static_cast<cudaStream_t>(stream)));
   return SPEC_OK;
 }
 

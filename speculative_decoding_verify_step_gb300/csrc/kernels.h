@@ -146,6 +146,7 @@ cudaError_t launch_accept_chain(const AcceptParams& p, bool sampled, PSource src
 // Acceptance of a model round from the LM head's per-tile statistics.
 constexpr int kDrawCluster = 8;
 constexpr int kMaxDrawCluster = 16;
+struct SelRow;
 struct RoundAcceptParams {
   int B, gamma, V;           // gamma: the widest window - 1 (stride of q, u, committed)
   const int32_t* seq_wlen;   // [B] window rows of sequence b
@@ -171,8 +172,40 @@ struct RoundAcceptParams {
   uint32_t* free_bits;
   int max_pages, max_batch;
   int* status;
+  // sampling adjustments (null: none): per window row, from the selection kernel
+  const SelRow* sel;
+  const float* sel_max;
+  const float* sel_z;
 };
 cudaError_t launch_accept_round(const RoundAcceptParams& p, bool sampled, cudaStream_t st);
+
+// ---------------------------------------------------------------- top-k / top-p
+constexpr int kSelCluster = 8;             // CTAs per probability row
+constexpr int kSelMaxSlice = 48 * 1024;    // probability keys per CTA (shared memory)
+struct SelectParams {
+  int V;
+  const int32_t* top_k;      // [sets] 0 (or >= V) = off
+  const float* top_p;        // [sets] 1 = off
+  // probabilities in, adjusted probabilities out (standalone): row r uses set r / rows_per_set
+  const float* p_in;
+  float* p_out;
+  int rows_per_set;
+  // model rounds: logits + LM-head tile statistics in, one SelRow per window row out
+  const float* logits;
+  const float* tstat_max;
+  const float* tstat_sum;
+  int n_tiles, tstat_stride;
+  float inv_temp;
+  const int32_t* seq_wlen;   // [B]
+  const int32_t* seq_rowoff; // [B]
+  SelRow* sel;               // [rows]
+  float* row_max;            // [rows] merged softmax statistics the acceptance reuses
+  float* row_z;
+  int* status;
+};
+int select_max_vocab();
+// kProbs: grid rows = n_rows; kLogits: n_rows_or_wmax = widest window, B sequences.
+cudaError_t launch_select(const SelectParams& p, PSource src, int n_rows_or_wmax, int B, cudaStream_t st);
 
 struct TreeParams {
   int B, N, V;

@@ -42,7 +42,8 @@ EXPORTS = ["spec_model_create", "spec_model_destroy", "spec_model_set_weight", "
            "spec_decode_step", "spec_verify_step", "spec_verify_tree_step", "spec_score", "spec_accept_probs",
            "spec_accept_greedy", "spec_get_kv_state", "spec_read_kv", "spec_debug_logits", "spec_kv_fill_random",
            "spec_sync_status", "spec_max_pages_per_seq", "spec_last_launch_count", "spec_last_error",
-           "spec_set_profiling", "spec_read_profile", "spec_accept_greedy_noalloc", "spec_verify_ragged"]
+           "spec_set_profiling", "spec_read_profile", "spec_accept_greedy_noalloc", "spec_verify_ragged",
+           "spec_adjust_probs"]
 
 RAGGED_CAP_ACCEPT, RAGGED_COMPACT = 1, 2
 
@@ -67,10 +68,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "spec_model_set_weight": (I32, [P, I32, I32, P, I64, P]),
         "spec_seq_reset": (I32, [P, I32, P, P]),
         "spec_prefill": (I32, [P, I32, P, P, I32, P, P]),
-        "spec_decode_step": (I32, [P, I32, P, P, F32, P, P, P]),
-        "spec_verify_step": (I32, [P, I32, I32, P, P, P, P, F32, P, P, P, P]),
+        "spec_decode_step": (I32, [P, I32, P, P, F32, P, P, P, P, P]),
+        "spec_verify_step": (I32, [P, I32, I32, P, P, P, P, F32, P, P, P, P, P, P]),
         "spec_verify_tree_step": (I32, [P, I32, I32, P, P, P, P, P, P, P]),
-        "spec_verify_ragged": (I32, [P, I32, I32, P, P, P, I32, I32, P, P, F32, P, P, P, P]),
+        "spec_verify_ragged": (I32, [P, I32, I32, P, P, P, I32, I32, P, P, F32, P, P, P, P, P, P]),
+        "spec_adjust_probs": (I32, [I32, I32, P, P, P, P, I32, P]),
         "spec_score": (I32, [P, I32, I32, P, P, P, P, P]),
         "spec_accept_probs": (I32, [I32, I32, I32, P, P, P, P, P, P, P, P]),
         "spec_accept_greedy": (I32, [I32, I32, I32, P, P, P, P, P, P]),
@@ -119,6 +121,20 @@ def _dev_i32(t, device) -> torch.Tensor:
     if not isinstance(t, torch.Tensor):
         t = torch.as_tensor(t)
     return t.to(device=device, dtype=torch.int32).contiguous()
+
+
+def _f32(t: Optional[torch.Tensor]) -> Optional[torch.Tensor]:
+    """q and u are fp32 on the C side: convert (no copy when already fp32 and contiguous)."""
+    return None if t is None else t.to(dtype=torch.float32).contiguous()
+
+
+def _opt_dev(t, device, dtype):
+    """None stays None (setting off); a list, array or tensor becomes a device tensor."""
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        t = torch.as_tensor(t)
+    return t.to(device=device, dtype=dtype).contiguous()
 
 
 class SpecModel:
@@ -173,17 +189,21 @@ class SpecModel:
                                  _stream()))
         torch.cuda.current_stream().synchronize()
 
-    def decode_step(self, seq_ids, tok, temperature: float = 0.0, u=None, out=None):
+    def decode_step(self, seq_ids, tok, temperature: float = 0.0, u=None, out=None, top_k=None, top_p=None):
         sid = _dev_i32(seq_ids, self.device)
         tk = _dev_i32(tok, self.device)
         B = sid.numel()
         out = torch.empty(B, dtype=torch.int32, device=self.device) if out is None else out
-        _check(_lib.spec_decode_step(self.handle, B, _ptr(sid), _ptr(tk), float(temperature), _ptr(u), _ptr(out),
-                                     _stream()))
+        kk, pp = _opt_dev(top_k, self.device, torch.int32), _opt_dev(top_p, self.device, torch.float32)
+        u = _f32(u)
+        _check(_lib.spec_decode_step(self.handle, B, _ptr(sid), _ptr(tk), float(temperature), _ptr(kk), _ptr(pp),
+                                     _ptr(u), _ptr(out), _stream()))
         return out
 
-    def verify_step(self, seq_ids, tok, q=None, u=None, temperature: float = 0.0, outs=None):
-        """tok [B, gamma+1] (pending + drafts).  Returns (accepted [B], committed [B, W], bonus [B])."""
+    def verify_step(self, seq_ids, tok, q=None, u=None, temperature: float = 0.0, outs=None, top_k=None,
+                    top_p=None):
+        """tok [B, gamma+1] (pending + drafts).  Returns (accepted [B], committed [B, W], bonus [B]).
+        top_k / top_p: per-sequence sampling adjustments of sampled rounds (None = off)."""
         sid = _dev_i32(seq_ids, self.device)
         tk = _dev_i32(tok, self.device)
         B, W = tk.shape
@@ -192,12 +212,15 @@ class SpecModel:
                     torch.empty(B, W, dtype=torch.int32, device=self.device),
                     torch.empty(B, dtype=torch.int32, device=self.device))
         acc, com, bon = outs
+        kk, pp = _opt_dev(top_k, self.device, torch.int32), _opt_dev(top_p, self.device, torch.float32)
+        q, u = _f32(q), _f32(u)
         _check(_lib.spec_verify_step(self.handle, B, W - 1, _ptr(sid), _ptr(tk), _ptr(q), _ptr(u),
-                                     float(temperature), _ptr(acc), _ptr(com), _ptr(bon), _stream()))
+                                     float(temperature), _ptr(kk), _ptr(pp), _ptr(acc), _ptr(com), _ptr(bon),
+                                     _stream()))
         return acc, com, bon
 
     def verify_ragged(self, seq_ids, tok, verify_lens, mode: int, q=None, u=None, temperature: float = 0.0,
-                      gamma: Optional[int] = None, outs=None):
+                      gamma: Optional[int] = None, outs=None, top_k=None, top_p=None):
         """mode RAGGED_CAP_ACCEPT: tok [B, gamma+1]; RAGGED_COMPACT: tok packed [sum(verify_lens)].
         verify_lens: per-sequence rows (list or tensor).  Returns (accepted, committed [B, gamma+1], bonus)."""
         sid = _dev_i32(seq_ids, self.device)
@@ -212,8 +235,11 @@ class SpecModel:
                     torch.empty(B, gamma + 1, dtype=torch.int32, device=self.device),
                     torch.empty(B, dtype=torch.int32, device=self.device))
         acc, com, bon = outs
+        kk, pp = _opt_dev(top_k, self.device, torch.int32), _opt_dev(top_p, self.device, torch.float32)
+        q, u = _f32(q), _f32(u)
         _check(_lib.spec_verify_ragged(self.handle, B, gamma, _ptr(sid), _ptr(tk), _ptr(lens), total, mode, _ptr(q),
-                                       _ptr(u), float(temperature), _ptr(acc), _ptr(com), _ptr(bon), _stream()))
+                                       _ptr(u), float(temperature), _ptr(kk), _ptr(pp), _ptr(acc), _ptr(com),
+                                       _ptr(bon), _stream()))
         return acc, com, bon
 
     def verify_tree_step(self, seq_ids, tok, parent: Sequence[int], outs=None):
@@ -300,6 +326,21 @@ def spec_accept_probs(p: torch.Tensor, q: Optional[torch.Tensor], x: Optional[to
                                  _ptr(bon), _stream()))
     torch.cuda.current_stream().synchronize()
     return acc, com, bon
+
+
+def spec_adjust_probs(p: torch.Tensor, top_k=None, top_p=None, rows_per_setting: int = 1, out=None):
+    """Top-k / top-p adjustment of probability rows p [..., V] (CUDA fp32); setting
+    i covers rows i*rows_per_setting .. (i+1)*rows_per_setting - 1 of the flattened
+    rows.  `out` may be p itself."""
+    lib = load_library()
+    V = p.shape[-1]
+    pp = p.float().contiguous()
+    rows = pp.numel() // V
+    out = torch.empty_like(pp) if out is None else out
+    kk, tp = _opt_dev(top_k, p.device, torch.int32), _opt_dev(top_p, p.device, torch.float32)
+    _check(lib.spec_adjust_probs(rows, V, _ptr(pp), _ptr(out), _ptr(kk), _ptr(tp), rows_per_setting, _stream()))
+    torch.cuda.current_stream().synchronize()
+    return out
 
 
 def spec_accept_greedy_noalloc(logits: torch.Tensor, x: Optional[torch.Tensor], outs=None):

@@ -157,3 +157,42 @@ def test_full_depth_page_tables_follow_the_oracle_allocator(full_depth):
         assert lens == kv.length
         np.testing.assert_array_equal(np.array(pt), kv.page_table_array([0, 1]))
     m.sync_status()
+
+
+def test_top1_and_nucleus_rounds_at_full_vocab(two_layer):
+    """V = 128256: a sampled round under top_k = 1 (or a vanishing nucleus) takes the
+    greedy round's decisions exactly; under top_k = 40 / top_p = 0.9 every committed
+    token of a sampled round lies in the kept set of its row."""
+    dims, w, m, o = two_layer
+    B, gamma = 4, 4
+    lens = [70, 90, 75, 81]
+    ids, prompts = _prefill_both(dims, m, o, lens, seed=11)
+    g = np.random.default_rng(12)
+    tok = torch.from_numpy(np.concatenate([np.array([[p[-1]] for p in prompts]),
+                                           g.integers(0, dims.vocab, (B, gamma))], axis=1)).int().cuda()
+    lg = m.score(ids, tok).cpu()
+    am = lg.argmax(-1)
+    tok[:, 1:3] = am[:, 0:2].int().cuda()            # some acceptance
+    lg = m.score(ids, tok)                            # scores of the final window
+    q = torch.from_numpy(synth.dirichlet1((B, gamma, dims.vocab), seed=2).numpy()).cuda()
+    u = torch.from_numpy(g.random((B, gamma + 1)).astype(np.float32)).cuda()
+
+    def fresh():
+        return _prefill_both(dims, m, o, lens, seed=11)[0]
+
+    a2, c2, _ = m.verify_step(fresh(), tok)
+    a1, c1, _ = m.verify_step(fresh(), tok, q=q, u=u, temperature=1.0, top_k=[1] * B)
+    assert torch.equal(a1, a2) and torch.equal(c1, c2)
+    a3, c3, _ = m.verify_step(fresh(), tok, q=q, u=u, temperature=1.0, top_p=[1e-7] * B)
+    assert torch.equal(a3, a2) and torch.equal(c3, c2)
+    a4, c4, _ = m.verify_step(fresh(), tok, q=q, u=u, temperature=1.0, top_k=[40] * B, top_p=[0.9] * B)
+    m.sync_status()
+    p = torch.softmax(lg.double(), -1)
+    for b in range(B):
+        n = int(a4[b])
+        row = p[b, n]
+        order = torch.argsort(row, descending=True, stable=True)
+        keep = order[:40]
+        c = torch.cumsum(row[keep], 0)
+        nuc = keep[:int((c < 0.9 * c[-1] * (1 - 1e-3)).sum()) + 2]   # the nucleus, with slack at the edge
+        assert int(c4[b, n]) in set(nuc.tolist())
