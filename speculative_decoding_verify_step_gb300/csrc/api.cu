@@ -114,9 +114,6 @@ struct spec_model {
   // workspaces
   float* resid = nullptr;
   act_t *xn = nullptr, *qrot = nullptr, *attn_out = nullptr, *act = nullptr;
-  float* part = nullptr;
-  long long part_elems = 0;
-  int* counters = nullptr;     // split-K tile counters (zero between launches)
   float *ssq_a = nullptr, *ssq_b = nullptr;  // [d/128][M_max] partial sums of r^2
   float* logits = nullptr;
   float *tstat_max = nullptr, *tstat_sum = nullptr;  // [V/128][M_max] LM-head tile statistics
@@ -231,13 +228,10 @@ spec_status forward(spec_model* m, int B, int W, const int32_t* seq_ids, const i
   const int BM = choose_bm(M);
   const int bi = bm_index(BM);
   auto splits_for = [&](int N, int K) {
-    const long long cap = m->part_elems / ((long long)M * N);
-    return choose_splits(N, K, M, BM, m->sm_count, (int)std::max(1LL, std::min(cap, 16LL)));
+    return choose_splits(N, K, M, BM, m->sm_count, 16);
   };
   EpiParams base{};
   base.M = M;
-  base.part = m->part;
-  base.counters = m->counters;
   base.ssq_tiles = d / 128;
   base.ssq_stride = m->M_max;
   base.inv_d = 1.f / d;
@@ -276,7 +270,6 @@ spec_status forward(spec_model* m, int B, int W, const int32_t* seq_ids, const i
       e.K = d;
       e.rscale = Ly.rs_qkv;
       e.splits = splits_for(e.N, e.K);
-      e.split_stride = (long long)M * e.N;
       e.ssq_in = m->ssq_a;
       e.Hq = Hq;
       e.Hkv = Hkv;
@@ -298,7 +291,6 @@ spec_status forward(spec_model* m, int B, int W, const int32_t* seq_ids, const i
       e.K = m->q_dim;
       e.rscale = Ly.rs_o;
       e.splits = splits_for(e.N, e.K);
-      e.split_stride = (long long)M * e.N;
       e.ssq_in = nullptr;
       e.resid = m->resid;
       e.g_next = Ly.ffn_norm;
@@ -313,7 +305,6 @@ spec_status forward(spec_model* m, int B, int W, const int32_t* seq_ids, const i
       e.K = d;
       e.rscale = Ly.rs_gu;
       e.splits = splits_for(e.N, e.K);
-      e.split_stride = (long long)M * e.N;
       e.ssq_in = m->ssq_b;
       e.act = m->act;
       e.ffn = F;
@@ -325,7 +316,6 @@ spec_status forward(spec_model* m, int B, int W, const int32_t* seq_ids, const i
       e.K = F;
       e.rscale = Ly.rs_down;
       e.splits = splits_for(e.N, e.K);
-      e.split_stride = (long long)M * e.N;
       e.ssq_in = nullptr;
       e.resid = m->resid;
       e.g_next = l + 1 < c.n_layers ? m->layers[l + 1].attn_norm : m->final_norm;
@@ -341,7 +331,6 @@ spec_status forward(spec_model* m, int B, int W, const int32_t* seq_ids, const i
     e.K = d;
     e.rscale = m->rs_lm;
     e.splits = 1;
-    e.split_stride = 0;
     e.ssq_in = m->ssq_a;
     e.logits = m->logits;
     e.inv_temp = inv_temp;
@@ -553,10 +542,6 @@ spec_status spec_model_create(const spec_config* cfg, spec_model** out) {
   ALLOC(m->qrot, (size_t)M_max * m->q_dim);
   ALLOC(m->attn_out, (size_t)m->M_alloc * m->q_dim);
   ALLOC(m->act, (size_t)m->M_alloc * F);
-  m->part_elems = std::max<long long>((long long)M_max * std::max({m->qkv_n, 2 * F, d}),
-                                      16LL * std::min(M_max, 64) * std::max({m->qkv_n, 2 * F, d}));
-  ALLOC(m->part, m->part_elems);
-  ALLOC(m->counters, (size_t)(std::max({m->qkv_n, 2 * F, d}) / 128) * ((M_max + 7) / 8));
   ALLOC(m->ssq_a, (size_t)(d / 128) * M_max);
   ALLOC(m->ssq_b, (size_t)(d / 128) * M_max);
   ALLOC(m->logits, (size_t)M_max * V);

@@ -260,6 +260,9 @@ __global__ void __launch_bounds__((kMaxRowTiles + 1) * 32)
           mma_f16_16816(acc[2 * dp + 1], a0, a1, a2, a3, b2, b3);
         }
       }
+      // The stage is refilled by TMA (async proxy) after this arrive: order this
+      // thread's ldmatrix reads (generic proxy) of it before that write.
+      fence_proxy_async();
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     }

@@ -120,6 +120,30 @@ SPEC_DEVICE_INLINE uint64_t l2_policy_evict_first() {
 
 // ------------------------------------------------ programmatic dependent launch
 // No-ops unless the kernel was launched with programmatic stream serialization.
+// ------------------------------------------------ thread-block cluster helpers
+// Cluster barrier in two halves: arrive (release: this thread's prior shared
+// memory writes become visible to the cluster) and wait (acquire).  Every thread
+// of every CTA in the cluster takes part, a whole warp at a time.
+SPEC_DEVICE_INLINE void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+SPEC_DEVICE_INLINE void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+
+// Shared-memory address `a` of this CTA mapped into the shared memory of cluster
+// rank `rank` (same offset there).
+SPEC_DEVICE_INLINE uint32_t mapa_u32(uint32_t a, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+  return r;
+}
+
+SPEC_DEVICE_INLINE float4 ld_dsmem_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
 SPEC_DEVICE_INLINE void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 SPEC_DEVICE_INLINE void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 

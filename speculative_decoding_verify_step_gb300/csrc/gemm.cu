@@ -13,10 +13,12 @@
 //   * eight consumer warps each own 16 weight rows and run mma.sync m16n8k16
 //     with the weights as the A operand ("swap-AB": weight rows on the MMA M
 //     side, token rows on N, so 1..64 tokens need no padding to 64);
-//   * split-K over gridDim.y fills the 152 SMs when N/128 tiles are few.  Each
-//     split writes its fp32 partial tile; the last split CTA of a tile to
-//     arrive (atomic tile counter, reset by that CTA) sums the partials in
-//     split order -- deterministic -- and applies the epilogue;
+//   * split-K over gridDim.y fills the 152 SMs when N/128 tiles are few.  The
+//     splits of a tile run as one thread-block cluster: each keeps its fp32
+//     partial tile in its own shared memory, and after a cluster barrier split r
+//     sums its share of the tile's rows over all splits through distributed
+//     shared memory, in split order -- deterministic -- and applies the
+//     epilogue to those rows;
 //   * the weight prefetch is issued before griddepcontrol.wait, so under
 //     programmatic dependent launch it overlaps the previous kernel's tail.
 //
@@ -25,6 +27,7 @@
 // each output row by s_m = rsqrt(sum r^2 / d + eps), since
 // sum_k (s_m r_mk g_k) W_nk = s_m sum_k (r_mk g_k) W_nk.
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 #include "launch.cuh"
@@ -39,6 +42,7 @@ constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;
 constexpr int kTilePad = kBN + 4;  // fp32 epilogue tile row pitch
+constexpr int kMaxSplits = 16;     // split-K cluster size limit (non-portable above 8)
 
 template <int BM>
 struct GemmCfg {
@@ -59,56 +63,43 @@ SPEC_DEVICE_INLINE void named_sync() {
 
 // The end of a tile, common to both projection kernels.  Called by the NT
 // epilogue threads (tid 0..NT-1, warp = tid / 32) once this CTA's accumulator is
-// in `tile` (splits == 1) or its partial is in p.part (splits > 1).  With split-K
-// the last CTA of the tile to arrive reduces the partials in split order, the
-// others return.  Then the row scales and the projection's epilogue.
+// in `tile` (its own shared memory).  With split-K the splits of a tile form one
+// thread-block cluster: after a cluster barrier, split r sums rows
+// [r * ROWS/S, (r+1) * ROWS/S) of all S partial tiles through distributed shared
+// memory, in split order (deterministic), and runs the epilogue on those rows --
+// the reduction is spread over the S CTAs and never leaves the chip.  The caller
+// holds back the CTA's exit with the matching cluster_wait().
 template <int EPI, int NT, int ROWS>
-SPEC_DEVICE_INLINE void finish_tile(const EpiParams& p, float* tile, float* s_scale, int* s_last, int m0, int n0,
-                                    int tid, int warp, int lane) {
+SPEC_DEVICE_INLINE void finish_tile(const EpiParams& p, float* tile, float* s_scale, int m0, int n0, int tid,
+                                    int warp, int lane) {
   constexpr int kGroupWarps = NT / 32;
+  int r_lo = 0, r_hi = min(ROWS, p.M - m0);
   if (p.splits > 1) {
-    __threadfence();
-    named_sync<NT>();
-    if (tid == 0) {
-      const int tile_id = blockIdx.z * gridDim.x + blockIdx.x;
-      const int prev = atomicAdd(&p.counters[tile_id], 1);
-      *s_last = prev == p.splits - 1;
-      if (*s_last) p.counters[tile_id] = 0;  // ready for the next launch
-    }
-    named_sync<NT>();
-    if (!*s_last) return;
-    __threadfence();
-    // sum the partials in split order (deterministic whichever CTA is last);
-    // 4 columns per thread, partials of 4 splits loaded before they are added
-    for (int e = tid; e < ROWS * (kBN / 4); e += NT) {
-      const int ml = e / (kBN / 4), cl = (e % (kBN / 4)) * 4;
-      const int m = m0 + ml;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (m < p.M) {
-        const float* src = p.part + (long long)m * p.N + n0 + cl;
-        int s = 0;
-        for (; s + 4 <= p.splits; s += 4) {
-          float4 a[4];
+    cluster_arrive();  // this CTA's partial tile is written
+    cluster_wait();    // ... and every other split's
+    const int S = p.splits, rank = blockIdx.y;
+    const int per = (ROWS + S - 1) / S;
+    r_lo = min(ROWS, rank * per);
+    r_hi = min(r_hi, r_lo + per);
+    for (int e = tid; e < max(0, r_hi - r_lo) * (kBN / 4); e += NT) {
+      const int ml = r_lo + e / (kBN / 4), cl = (e % (kBN / 4)) * 4;
+      const uint32_t off = smem_u32(tile + ml * kTilePad + cl);
+      float4 a[kMaxSplits];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) a[j] = __ldcg(reinterpret_cast<const float4*>(src + (s + j) * p.split_stride));
+      for (int j = 0; j < kMaxSplits; ++j)
+        if (j < S) a[j] = ld_dsmem_f4(mapa_u32(off, j));
+      float4 v = a[0];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            v.x += a[j].x;
-            v.y += a[j].y;
-            v.z += a[j].z;
-            v.w += a[j].w;
-          }
+      for (int j = 1; j < kMaxSplits; ++j)
+        if (j < S) {
+          v.x += a[j].x;
+          v.y += a[j].y;
+          v.z += a[j].z;
+          v.w += a[j].w;
         }
-        for (; s < p.splits; ++s) {
-          const float4 a = __ldcg(reinterpret_cast<const float4*>(src + s * p.split_stride));
-          v.x += a.x;
-          v.y += a.y;
-          v.z += a.z;
-          v.w += a.w;
-        }
-      }
       *reinterpret_cast<float4*>(&tile[ml * kTilePad + cl]) = v;
     }
+    cluster_arrive();  // done reading the other CTAs' tiles
   }
   // weight-row scale 2^-e of the fp16 encoding, per output column of the tile
   __shared__ float s_rs[kBN];
@@ -117,10 +108,10 @@ SPEC_DEVICE_INLINE void finish_tile(const EpiParams& p, float* tile, float* s_sc
   // One warp per row, one tile partial per lane (independent loads, then a fixed
   // shuffle tree: the same order on every run).
 #pragma unroll 4
-  for (int r = warp; r < ROWS; r += kGroupWarps) {
+  for (int r = r_lo + warp; r < r_hi; r += kGroupWarps) {
     const int m = m0 + r;
     float sc = 1.f;
-    if (p.ssq_in && m < p.M) {
+    if (p.ssq_in) {
       float ss = 0.f;
       for (int t = lane; t < p.ssq_tiles; t += 32) ss += __ldcg(p.ssq_in + (long long)t * p.ssq_stride + m);
       ss = warp_sum(ss);
@@ -133,10 +124,9 @@ SPEC_DEVICE_INLINE void finish_tile(const EpiParams& p, float* tile, float* s_sc
   if constexpr (EPI == kEpiQKV) {
     // tile = 128 fused-QKV columns (one head of 128, or two of 64); RoPE pairs (i, i + hd/2)
     const int half = p.hd >> 1;
-    for (int e = tid; e < ROWS * (kBN / 2); e += NT) {
-      const int ml = e / (kBN / 2), pr = e % (kBN / 2);
+    for (int e = tid; e < max(0, r_hi - r_lo) * (kBN / 2); e += NT) {
+      const int ml = r_lo + e / (kBN / 2), pr = e % (kBN / 2);
       const int m = m0 + ml;
-      if (m >= p.M) continue;
       const int cl = (pr / half) * p.hd + pr % half;
       const int n = n0 + cl;
       const int head = n / p.hd, i = n % p.hd;
@@ -170,10 +160,9 @@ SPEC_DEVICE_INLINE void finish_tile(const EpiParams& p, float* tile, float* s_sc
   } else if constexpr (EPI == kEpiSwiGLU) {
     // tile = 64 gate rows then the 64 up rows of the same features
     const int f0 = (n0 / kBN) * 64;
-    for (int e = tid; e < ROWS * 64; e += NT) {
-      const int ml = e / 64, fl = e % 64;
+    for (int e = tid; e < max(0, r_hi - r_lo) * 64; e += NT) {
+      const int ml = r_lo + e / 64, fl = e % 64;
       const int m = m0 + ml;
-      if (m >= p.M) continue;
       const float sc = s_scale[ml];
       const float gv = tile[ml * kTilePad + fl] * (sc * s_rs[fl]);
       const float uv = tile[ml * kTilePad + 64 + fl] * (sc * s_rs[64 + fl]);
@@ -183,9 +172,8 @@ SPEC_DEVICE_INLINE void finish_tile(const EpiParams& p, float* tile, float* s_sc
   } else if constexpr (EPI == kEpiResid) {
     // r += y; next input X' = fp16(r * g_next); per-tile sum of r^2 for the next norm.
     // Warp w handles rows w, w+8, ...; lane covers columns lane + 32j (fixed order).
-    for (int ml = warp; ml < ROWS; ml += kGroupWarps) {
+    for (int ml = r_lo + warp; ml < r_hi; ml += kGroupWarps) {
       const int m = m0 + ml;
-      if (m >= p.M) continue;
       float ss = 0.f;
 #pragma unroll
       for (int j = 0; j < kBN / 32; ++j) {
@@ -200,9 +188,8 @@ SPEC_DEVICE_INLINE void finish_tile(const EpiParams& p, float* tile, float* s_sc
       if (lane == 0) p.ssq_out[(long long)(n0 / kBN) * p.ssq_stride + m] = ss;
     }
   } else {  // kEpiLogits: logits = s_m * y, plus per-tile softmax statistics of each row
-    for (int ml = warp; ml < ROWS; ml += kGroupWarps) {
+    for (int ml = r_lo + warp; ml < r_hi; ml += kGroupWarps) {
       const int m = m0 + ml;
-      if (m >= p.M) continue;
       const float sc = s_scale[ml];
       float v[kBN / 32];
       float mx = -INFINITY;
@@ -253,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kPipeBytes);
   uint64_t* empty = full + C::kStages;
   float* s_scale = reinterpret_cast<float*>(empty + C::kStages);
-  __shared__ int s_last, s_fail;
+  __shared__ int s_fail;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -298,6 +285,13 @@ __global__ void __launch_bounds__(kThreads, 2)
         tma_load_2d_hint(stage_w(s), &tmW, (kb0 + kb) * kBK, n0, &full[s], pol);
         tma_load_2d(stage_x(s), &tmX, (kb0 + kb) * kBK, m0, &full[s]);
       }
+    }
+    __syncwarp();
+    if (p.splits > 1) {  // the two cluster barriers of the split-K reduction
+      cluster_arrive();
+      cluster_wait();
+      cluster_arrive();
+      cluster_wait();
     }
     return;
   }
@@ -345,6 +339,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
       }
     }
+    // The stage is refilled by TMA (async proxy) after this arrive: order this
+    // thread's ldmatrix reads (generic proxy) of it before that write.
+    fence_proxy_async();
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
   }
@@ -354,36 +351,29 @@ __global__ void __launch_bounds__(kThreads, 2)
   float* tile = reinterpret_cast<float*>(smem);  // reuses the (now idle) pipeline buffers
   if (!ok) s_fail = 1;
   named_sync<kConsumers>();
-  if (s_fail) return;
+  if (s_fail) {
+    if (p.splits > 1) {  // still take part in the cluster barriers
+      cluster_arrive();
+      cluster_wait();
+      cluster_arrive();
+      cluster_wait();
+    }
+    return;
+  }
 
   // acc[t] = D tile (16 weight rows x 8 tokens): d0,d1 -> (row g, tokens 2c, 2c+1),
   // d2,d3 -> (row g+8, same tokens).  Rows of the output tile = tokens.
-  if (p.splits == 1) {
 #pragma unroll
-    for (int t = 0; t < BM / 8; ++t) {
-      const int ml = t * 8 + 2 * c;
-      tile[ml * kTilePad + wrow + g] = acc[t][0];
-      tile[ml * kTilePad + wrow + g + 8] = acc[t][2];
-      tile[(ml + 1) * kTilePad + wrow + g] = acc[t][1];
-      tile[(ml + 1) * kTilePad + wrow + g + 8] = acc[t][3];
-    }
-  } else {
-    float* out = p.part + (long long)split * p.split_stride;
-    const int n = n0 + wrow + g;
-#pragma unroll
-    for (int t = 0; t < BM / 8; ++t) {
-      const int m = m0 + t * 8 + 2 * c;
-      if (m < p.M) {
-        out[(long long)m * p.N + n] = acc[t][0];
-        out[(long long)m * p.N + n + 8] = acc[t][2];
-      }
-      if (m + 1 < p.M) {
-        out[(long long)(m + 1) * p.N + n] = acc[t][1];
-        out[(long long)(m + 1) * p.N + n + 8] = acc[t][3];
-      }
-    }
+  for (int t = 0; t < BM / 8; ++t) {
+    const int ml = t * 8 + 2 * c;
+    tile[ml * kTilePad + wrow + g] = acc[t][0];
+    tile[ml * kTilePad + wrow + g + 8] = acc[t][2];
+    tile[(ml + 1) * kTilePad + wrow + g] = acc[t][1];
+    tile[(ml + 1) * kTilePad + wrow + g + 8] = acc[t][3];
   }
-  finish_tile<EPI, kConsumers, BM>(p, tile, s_scale, &s_last, m0, n0, tid, warp, lane);
+  named_sync<kConsumers>();
+  finish_tile<EPI, kConsumers, BM>(p, tile, s_scale, m0, n0, tid, warp, lane);
+  if (p.splits > 1) cluster_wait();  // the other splits are done reading this CTA's tile
 }
 
 
@@ -423,7 +413,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* accum = empty + C::kStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
   float* s_scale = reinterpret_cast<float*>(tmem_slot + 4);
-  __shared__ int s_last, s_fail;
+  __shared__ int s_fail;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -512,21 +502,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (!done) s_fail = 1;
     float* tile = reinterpret_cast<float*>(smem);  // MMAs and loads are done with the stages
     if (done) {
-      float* out = p.part + (long long)split * p.split_stride;
 #pragma unroll 1
       for (int c0 = 0; c0 < NT; c0 += 16) {
         float v[16];
         tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + c0, v);
-        if (p.splits == 1) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) tile[(c0 + i) * kTilePad + nl] = v[i];
-        } else {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int m = m0 + c0 + i;
-            if (m < p.M) out[(long long)m * p.N + n0 + nl] = v[i];
-          }
-        }
+        for (int i = 0; i < 16; ++i) tile[(c0 + i) * kTilePad + nl] = v[i];
       }
     }
     tc_fence_before();
@@ -538,50 +519,107 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
-  if (s_fail) return;
+  if (s_fail) {
+    if (p.splits > 1) {  // still take part in the cluster barriers
+      cluster_arrive();
+      cluster_wait();
+      cluster_arrive();
+      cluster_wait();
+    }
+    return;
+  }
   if (warp < 2) pdl_wait();  // outputs are written below by every warp
-  finish_tile<EPI, kTcThreads, NT>(p, reinterpret_cast<float*>(smem), s_scale, &s_last, m0, n0, threadIdx.x, warp,
-                                   lane);
+  finish_tile<EPI, kTcThreads, NT>(p, reinterpret_cast<float*>(smem), s_scale, m0, n0, threadIdx.x, warp, lane);
+  if (p.splits > 1) cluster_wait();  // the other splits are done reading this CTA's tile
 }
 
-template <int NT, int EPI>
-cudaError_t launch_tc(const CUtensorMap* tmW, const CUtensorMap* tmX, const EpiParams& p, cudaStream_t st) {
-  using C = TcCfg<NT>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e =
-        cudaFuncSetAttribute(gemm_tc_kernel<NT, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured = true;
+// Kernel, block size and dynamic shared memory of the projection for a token tile.
+template <int BM, int EPI>
+struct Kern {
+  static constexpr bool kTc = BM > 64;
+  static auto fn() {
+    if constexpr (kTc) {
+      return gemm_tc_kernel<BM, EPI>;
+    } else {
+      return gemm_swapab_kernel<BM, EPI>;
+    }
   }
-  dim3 grid(p.N / kBN, p.splits, (p.M + NT - 1) / NT);
-  return launch_k(gemm_tc_kernel<NT, EPI>, grid, dim3(kTcThreads), C::kSmemBytes, st, *tmW, *tmX, p);
-}
+  static constexpr int kThreadsPerCta = kTc ? kTcThreads : kThreads;
+  static constexpr int kSmem = kTc ? TcCfg<kTc ? BM : 128>::kSmemBytes : GemmCfg<kTc ? 8 : BM>::kSmemBytes;
+};
 
 template <int BM, int EPI>
-cudaError_t launch_bm(const CUtensorMap* tmW, const CUtensorMap* tmX, const EpiParams& p, cudaStream_t st) {
-  using C = GemmCfg<BM>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_swapab_kernel<BM, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+cudaError_t configure() {
+  static bool done = false;
+  if (done) return cudaSuccess;
+  using K = Kern<BM, EPI>;
+  cudaError_t e = cudaFuncSetAttribute(K::fn(), cudaFuncAttributeMaxDynamicSharedMemorySize, K::kSmem);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(K::fn(), cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e == cudaSuccess) done = true;
+  return e;
+}
+
+// Split-K runs each tile's splits as one cluster of (1, splits, 1) CTAs.
+template <int BM, int EPI>
+cudaError_t launch_proj(const CUtensorMap* tmW, const CUtensorMap* tmX, const EpiParams& p, cudaStream_t st) {
+  using K = Kern<BM, EPI>;
+  if (cudaError_t e = configure<BM, EPI>()) return e;
   dim3 grid(p.N / kBN, p.splits, (p.M + BM - 1) / BM);
-  return launch_k(gemm_swapab_kernel<BM, EPI>, grid, dim3(kThreads), C::kSmemBytes, st, *tmW, *tmX, p);
+  if (p.splits == 1) return launch_k(K::fn(), grid, dim3(K::kThreadsPerCta), K::kSmem, st, *tmW, *tmX, p);
+  return launch_k_cluster(K::fn(), grid, dim3(K::kThreadsPerCta), K::kSmem, st, dim3(1, p.splits, 1), *tmW, *tmX,
+                          p);
+}
+
+// How many (1, s, 1) clusters of the projection kernel fit on the GPU at once.
+template <int BM>
+int max_active_clusters(int s) {
+  static std::mutex mu;
+  static int cache[kMaxSplits + 1] = {};
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[s] == 0) {
+    using K = Kern<BM, kEpiResid>;
+    int n = 0;
+    if (configure<BM, kEpiResid>() == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(1, s, 1);
+      cfg.blockDim = dim3(K::kThreadsPerCta);
+      cfg.dynamicSmemBytes = K::kSmem;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 1;
+      attr[0].val.clusterDim.y = s;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&n, K::fn(), &cfg) != cudaSuccess) n = 0;
+    }
+    (void)cudaGetLastError();
+    cache[s] = n > 0 ? n : -1;
+  }
+  return cache[s];
+}
+
+int max_active_clusters_bm(int BM, int s) {
+  switch (BM) {
+    case 8: return max_active_clusters<8>(s);
+    case 16: return max_active_clusters<16>(s);
+    case 32: return max_active_clusters<32>(s);
+    case 64: return max_active_clusters<64>(s);
+    case 128: return max_active_clusters<128>(s);
+    default: return max_active_clusters<256>(s);
+  }
 }
 
 template <int EPI>
 cudaError_t launch_epi(const CUtensorMap* tmW, const CUtensorMap* tmX, int BM, const EpiParams& p,
                        cudaStream_t st) {
   switch (BM) {  // up to 64 token rows: mma.sync (HBM-bound); above: tcgen05
-    case 8: return launch_bm<8, EPI>(tmW, tmX, p, st);
-    case 16: return launch_bm<16, EPI>(tmW, tmX, p, st);
-    case 32: return launch_bm<32, EPI>(tmW, tmX, p, st);
-    case 64: return launch_bm<64, EPI>(tmW, tmX, p, st);
-    case 128: return launch_tc<128, EPI>(tmW, tmX, p, st);
-    case 256: return launch_tc<256, EPI>(tmW, tmX, p, st);
+    case 8: return launch_proj<8, EPI>(tmW, tmX, p, st);
+    case 16: return launch_proj<16, EPI>(tmW, tmX, p, st);
+    case 32: return launch_proj<32, EPI>(tmW, tmX, p, st);
+    case 64: return launch_proj<64, EPI>(tmW, tmX, p, st);
+    case 128: return launch_proj<128, EPI>(tmW, tmX, p, st);
+    case 256: return launch_proj<256, EPI>(tmW, tmX, p, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -598,16 +636,20 @@ int choose_bm(int M) {
 }
 
 int choose_splits(int N, int K, int M, int BM, int sm_count, int max_splits) {
-  // One wave: as many CTAs as fit at once (shared memory allows two per SM up to
-  // 64 token rows, one above), so every split of a tile is resident together and
-  // no tile's reduction waits for a second wave.
+  // The most splits (cluster size) for which every tile's cluster is resident in
+  // one wave (shared memory allows two CTAs per SM up to 128 token rows, one
+  // above; the GPC layout limits how many clusters fit), with every split
+  // non-empty and at least 4 k-blocks long.
   const int tiles = (N / kBN) * ((M + BM - 1) / BM);
   const int kb = K / kBK;
   const int slots = (BM <= 128 ? 2 : 1) * sm_count;
-  int s = std::max(1, slots / tiles);
-  s = std::min(s, std::min(max_splits, std::max(1, kb / 4)));
-  const int per = (kb + s - 1) / s;  // make every split non-empty
-  return (kb + per - 1) / per;
+  const int smax = std::min({max_splits, kMaxSplits, std::max(1, kb / 4), std::max(1, slots / tiles)});
+  for (int s = smax; s > 1; --s) {
+    const int per = (kb + s - 1) / s;
+    if ((kb + per - 1) / per != s) continue;  // some split would be empty
+    if (tiles <= max_active_clusters_bm(BM, s)) return s;
+  }
+  return 1;
 }
 
 cudaError_t launch_gemm_epi(int epi, const CUtensorMap* tmW, const CUtensorMap* tmX, int BM, EpiParams p,

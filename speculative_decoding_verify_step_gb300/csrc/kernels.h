@@ -18,16 +18,13 @@ void record_error(const char* msg);
 
 // Fused-epilogue projection (gemm.cu).  Y = X W^T over M rows; W: [N, K] fp16 with
 // a per-row scale (tensor map box {64, 128}), X: [M_alloc, K] fp16 (box {64, BM}).
-// split-K partials land in `part` ([splits][M][N] fp32); the last split CTA of a
-// tile reduces them and applies the epilogue:
+// With split-K the splits of a tile run as one thread-block cluster and reduce
+// their partial tiles through distributed shared memory before the epilogue:
 enum { kEpiQKV = 0, kEpiSwiGLU = 1, kEpiResid = 2, kEpiLogits = 3 };
 struct EpiParams {
   int M, N, K;
   int kb_total, kb_per_split, splits;  // kb_* filled by the launcher
   const float* rscale;                 // [N] 2^-e of each weight row's fp16 encoding
-  float* part;
-  long long split_stride;
-  int* counters;                       // one per (m tile, n tile), zero between launches
   // row scale of a normalised input (ssq_in = null: scale 1)
   const float* ssq_in;                 // [ssq_tiles][ssq_stride] partial sums of r^2
   int ssq_tiles, ssq_stride;

@@ -196,3 +196,18 @@ def test_top1_and_nucleus_rounds_at_full_vocab(two_layer):
         c = torch.cumsum(row[keep], 0)
         nuc = keep[:int((c < 0.9 * c[-1] * (1 - 1e-3)).sum()) + 2]   # the nucleus, with slack at the edge
         assert int(c4[b, n]) in set(nuc.tolist())
+
+
+@pytest.mark.parametrize("B,W", [(1, 16), (4, 8)])
+def test_repeated_scores_are_bit_identical(two_layer, B, W):
+    """Every reduction of the path runs in a fixed order, so scoring the same window
+    again gives the same bits.  Catches pipeline races (a stage refilled while it is
+    still being read shows up as a few wrong weight rows in one tile)."""
+    dims, w, m, o = two_layer
+    ids, prompts = _prefill_both(dims, m, o, [70 + 9 * b for b in range(B)], seed=21)
+    g = np.random.default_rng(22)
+    tok = torch.from_numpy(np.concatenate([np.array([[p[-1]] for p in prompts]),
+                                           g.integers(0, dims.vocab, (B, W - 1))], axis=1)).int().cuda()
+    first = m.score(ids, tok).clone()
+    for _ in range(20):
+        assert torch.equal(m.score(ids, tok), first)
