@@ -255,6 +255,7 @@ spec_status forward(spec_model* m, int B, int W, const int32_t* seq_ids, const i
   for (int j = 0; j < 16; ++j) ap.anc[j] = j < W ? anc[j] : 0u;
   ap.out = m->attn_out;
   ap.sm_count = m->sm_count;
+  ap.kv_len_hint = (int)std::min<long long>(max_len_bound(m) + W, c.max_seq_len);
   ap.status = m->status;
 
   const long long layer_elems = (long long)c.num_pages * Hkv * kPage * hd;

@@ -14,8 +14,12 @@
 //
 // K/V pages (64 tokens x head_dim fp16 per kv head) are streamed by TMA with
 // the 128-byte swizzle into a 3-stage mbarrier pipeline fed by one producer
-// warp; consumer warps (16 query rows each) run QK^T and PV on mma.sync with
-// an online softmax in fp32 (exp2 domain).  A sequence's pages are split over a
+// warp.  Consumer warps are (row tile, key group) pairs: a warp owns 16 query
+// rows and 64/KG keys of every page, runs QK^T and PV on mma.sync with an online
+// softmax in fp32 (exp2 domain), and the KG partials of a row tile are combined
+// in shared memory at the end.  Splitting the keys of a page over KG warps puts
+// a warp on every scheduler, so the short dependent MMA chains of a 16-row tile
+// overlap instead of running back to back.  A sequence's pages are split over a
 // thread-block cluster of 8 CTAs; each CTA leaves its partial (unnormalised O,
 // running max, running sum) in its own shared memory and the cluster merges
 // them through distributed shared memory with log-sum-exp weights, so the
@@ -33,7 +37,19 @@ namespace spec {
 namespace {
 
 constexpr int kAttnStages = 3;
-constexpr int kMaxRowTiles = 4;  // up to 64 query rows (W * group) per CTA
+constexpr int kMaxRowTiles = 4;       // up to 64 query rows (W * group) per CTA
+constexpr int kMaxConsumerWarps = 4;  // row tiles x key groups
+constexpr int kMaxKgSlots = 3;        // partials of key groups > 0 (row tiles x (KG - 1))
+
+// Key groups per page for a launch with `row_tiles` row tiles: four consumer warps
+// at most, so a CTA stays small enough for several to share an SM.  Splitting keys
+// pays off only when a CTA has pages enough to amortise the final combine (measured
+// on GB300: from about 4 pages per CTA with one row tile, 8 with two).
+inline int key_groups(int row_tiles, int pages_per_cta) {
+  if (row_tiles == 1 && pages_per_cta >= 4) return 4;
+  if (row_tiles == 2 && pages_per_cta >= 8) return 2;
+  return 1;
+}
 
 template <int HD>
 struct AttnCfg {
@@ -43,8 +59,8 @@ struct AttnCfg {
   static constexpr int kSmemBytes = kAttnStages * kStageBytes + 2 * kAttnStages * 8 + 1024;
 };
 
-template <int HD, int CS>
-__global__ void __launch_bounds__((kMaxRowTiles + 1) * 32)
+template <int HD, int CS, int KG>
+__global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32)
     attention_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                      const __grid_constant__ AttnParams p) {
   using C = AttnCfg<HD>;
@@ -60,8 +76,9 @@ __global__ void __launch_bounds__((kMaxRowTiles + 1) * 32)
   const int b = blockIdx.z;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int n_row_tiles = blockDim.x / 32 - 1;
+  const int n_cons = blockDim.x / 32 - 1;  // consumer warps: (row tile, key group) pairs
   const int grp = p.Hq / p.Hkv;
+  constexpr int KT = 4 / KG;                // 16-key tiles of a page per consumer warp
 
   // Sequence state and the cached pages were written by kernels that completed
   // before the QKV projection (this kernel's predecessor) passed its own
@@ -86,7 +103,7 @@ __global__ void __launch_bounds__((kMaxRowTiles + 1) * 32)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kAttnStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], n_row_tiles);
+      mbar_init(&empty[s], n_cons);
     }
     s_fail = 0;
     fence_barrier_init();
@@ -97,8 +114,18 @@ __global__ void __launch_bounds__((kMaxRowTiles + 1) * 32)
   float* part_o = reinterpret_cast<float*>(smem);            // [rows][HD]
   float* part_m = part_o + kMaxRowTiles * 16 * HD;           // [rows]
   float* part_l = part_m + kMaxRowTiles * 16;                // [rows]
+  float* wts = part_l + kMaxRowTiles * 16;                   // [rows per CTA][CS] merge weights
+  float* kg_o = wts + kMaxRowTiles * 16 * 16;                // [slots][16][HD] key-group partials
+  float* kg_m = kg_o + kMaxKgSlots * 16 * HD;                // [slots][16]
+  float* kg_l = kg_m + kMaxKgSlots * 16;
+  float* kg_w = kg_l + kMaxKgSlots * 16;                     // [rows][KG] combine weights
+  float* cm = kg_w + kMaxRowTiles * 16 * 4;                  // [rows] combined max, sum
+  float* cl = cm + kMaxRowTiles * 16;
+  static_assert((kMaxRowTiles * 16 * (HD + 2 + 16 + 4 + 2) + kMaxKgSlots * 16 * (HD + 2)) * 4 <=
+                    kAttnStages * 2 * kPage * HD * 2,
+                "partials fit in the stage buffers");
 
-  if (warp == n_row_tiles) {
+  if (warp == n_cons) {
     // --------------------------------------------------------------- producer
     if (lane == 0 && npg > 0) {
       tma_prefetch_desc(&tmK);
@@ -133,12 +160,13 @@ __global__ void __launch_bounds__((kMaxRowTiles + 1) * 32)
     // ---------------------------------------------------------------- consumers
     pdl_wait();  // q is written by the QKV projection
     const int g = lane >> 2, c = lane & 3;
-    // query rows of this thread: r0 = warp*16 + g, r1 = r0 + 8; row r -> window row j = r / grp
+    const int rt = warp / KG, kg = warp % KG;  // row tile, key group (keys kg*16*KT .. of each page)
+    // query rows of this thread: r0 = rt*16 + g, r1 = r0 + 8; row r -> window row j = r / grp
     int jrow[2], head[2];
     bool valid[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const int r = warp * 16 + g + 8 * h;
+      const int r = rt * 16 + g + 8 * h;
       valid[h] = r < rows;
       jrow[h] = valid[h] ? r / grp : 0;
       head[h] = kvh * grp + (valid[h] ? r % grp : 0);
@@ -177,15 +205,15 @@ __global__ void __launch_bounds__((kMaxRowTiles + 1) * 32)
       const uint32_t kbase = smem_u32(smem + s * C::kStageBytes);
       const uint32_t vbase = kbase + C::kTileBytes;
 
-      // S = Q K^T for the page's 64 keys: 8 key tiles of 8
-      float sc[8][4];
+      // S = Q K^T for this warp's 16*KT keys of the page: 2*KT key tiles of 8
+      float sc[2 * KT][4];
 #pragma unroll
-      for (int t = 0; t < 8; ++t) sc[t][0] = sc[t][1] = sc[t][2] = sc[t][3] = 0.f;
+      for (int t = 0; t < 2 * KT; ++t) sc[t][0] = sc[t][1] = sc[t][2] = sc[t][3] = 0.f;
 #pragma unroll
       for (int ks = 0; ks < HD / 16; ++ks) {
 #pragma unroll
-        for (int tp = 0; tp < 4; ++tp) {
-          const int key = tp * 16 + (lane & 7) + ((lane >> 4) & 1) * 8;
+        for (int tp = 0; tp < KT; ++tp) {
+          const int key = (kg * KT + tp) * 16 + (lane & 7) + ((lane >> 4) & 1) * 8;
           const int d = ks * 16 + ((lane >> 3) & 1) * 8;
           uint32_t b0, b1, b2, b3;
           ldsm_x4(kbase + (d >> 6) * (kPage * 128) + swz128(key, d & 63), b0, b1, b2, b3);
@@ -194,10 +222,10 @@ __global__ void __launch_bounds__((kMaxRowTiles + 1) * 32)
         }
       }
       // mask + online softmax (exp2 domain)
-      const int key0 = (pg0 + i) * kPage;
+      const int key0 = (pg0 + i) * kPage + kg * KT * 16;
       float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-      for (int t = 0; t < 8; ++t) {
+      for (int t = 0; t < 2 * KT; ++t) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int h = e >> 1;
@@ -221,7 +249,7 @@ __global__ void __launch_bounds__((kMaxRowTiles + 1) * 32)
       }
       float rs[2] = {0.f, 0.f};
 #pragma unroll
-      for (int t = 0; t < 8; ++t) {
+      for (int t = 0; t < 2 * KT; ++t) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int h = e >> 1;
@@ -245,14 +273,14 @@ __global__ void __launch_bounds__((kMaxRowTiles + 1) * 32)
       }
       // O += P V: P from the score registers (fp16), V via transposed ldmatrix
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
+      for (int kk = 0; kk < KT; ++kk) {
         const uint32_t a0 = pack_f16x2(sc[2 * kk][0], sc[2 * kk][1]);
         const uint32_t a1 = pack_f16x2(sc[2 * kk][2], sc[2 * kk][3]);
         const uint32_t a2 = pack_f16x2(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
         const uint32_t a3 = pack_f16x2(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
 #pragma unroll
         for (int dp = 0; dp < HD / 16; ++dp) {
-          const int key = kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+          const int key = (kg * KT + kk) * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
           const int d = dp * 16 + ((lane >> 4) & 1) * 8;
           uint32_t b0, b1, b2, b3;
           ldsm_x4_trans(vbase + (d >> 6) * (kPage * 128) + swz128(key, d & 63), b0, b1, b2, b3);
@@ -268,30 +296,71 @@ __global__ void __launch_bounds__((kMaxRowTiles + 1) * 32)
     }
     // drained: every issued page was consumed, so the stage buffers are free
     // once all consumer warps are here (named barrier over the consumers)
-    asm volatile("bar.sync 1, %0;" ::"r"(n_row_tiles * 32) : "memory");
+    asm volatile("bar.sync 1, %0;" ::"r"(n_cons * 32) : "memory");
+    // key group 0 writes straight into the CTA partial, the others into slots
+    const int slot = rt * (KG - 1) + kg - 1;
+    float* o_dst = kg == 0 ? part_o : kg_o + slot * 16 * HD - rt * 16 * HD;
+    float* m_dst = kg == 0 ? part_m : kg_m + slot * 16 - rt * 16;
+    float* l_dst = kg == 0 ? part_l : kg_l + slot * 16 - rt * 16;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const int r = warp * 16 + g + 8 * h;
+      const int r = rt * 16 + g + 8 * h;
 #pragma unroll
       for (int t = 0; t < HD / 8; ++t) {
-        part_o[r * HD + t * 8 + 2 * c] = acc[t][2 * h];
-        part_o[r * HD + t * 8 + 2 * c + 1] = acc[t][2 * h + 1];
+        o_dst[r * HD + t * 8 + 2 * c] = acc[t][2 * h];
+        o_dst[r * HD + t * 8 + 2 * c + 1] = acc[t][2 * h + 1];
       }
       if (c == 0) {
-        part_m[r] = valid[h] ? mrow[h] : -INFINITY;
-        part_l[r] = valid[h] ? lrow[h] : 0.f;
+        m_dst[r] = valid[h] ? mrow[h] : -INFINITY;
+        l_dst[r] = valid[h] ? lrow[h] : 0.f;
       }
+    }
+    if constexpr (KG > 1) {
+    asm volatile("bar.sync 1, %0;" ::"r"(n_cons * 32) : "memory");
+    // combine the KG partials of every row: weights 2^(m_kg - max m), then O, m, l
+    const int n_rows_launch = (n_cons / KG) * 16;
+    const int ctid = threadIdx.x;  // consumer threads are 0 .. n_cons*32-1
+    for (int r = ctid; r < n_rows_launch; r += n_cons * 32) {
+      const int t = r / 16, rr = r % 16;
+      float mk[KG], mt = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < KG; ++k) {
+        mk[k] = k == 0 ? part_m[r] : kg_m[(t * (KG - 1) + k - 1) * 16 + rr];
+        mt = fmaxf(mt, mk[k]);
+      }
+      float lt = 0.f;
+#pragma unroll
+      for (int k = 0; k < KG; ++k) {
+        const float wk = (mt == -INFINITY || mk[k] == -INFINITY) ? 0.f : exp2f(mk[k] - mt);
+        kg_w[r * 4 + k] = wk;
+        lt += wk * (k == 0 ? part_l[r] : kg_l[(t * (KG - 1) + k - 1) * 16 + rr]);
+      }
+      cm[r] = mt;
+      cl[r] = lt;
+    }
+    asm volatile("bar.sync 1, %0;" ::"r"(n_cons * 32) : "memory");
+    for (int e = ctid; e < n_rows_launch * HD; e += n_cons * 32) {
+      const int r = e / HD, d = e % HD;
+      const int t = r / 16, rr = r % 16;
+      float o = kg_w[r * 4] * part_o[e];
+#pragma unroll
+      for (int k = 1; k < KG; ++k) o += kg_w[r * 4 + k] * kg_o[((t * (KG - 1) + k - 1) * 16 + rr) * HD + d];
+      part_o[e] = o;
+      if (d == 0) {
+        part_m[r] = cm[r];
+        part_l[r] = cl[r];
+      }
+    }
     }
   }
   // every CTA of the cluster has its partials in shared memory
-  if (warp == n_row_tiles) pdl_wait();  // every thread below may write the output
+  if (warp == n_cons) pdl_wait();  // every thread below may write the output
   cluster.sync();
   if (!s_fail) {
     // CTA `rank` merges rows rank, rank + 8, ...  First the per-row weights
     // w_s = 2^(m_s - max m) / sum_s 2^(m_s - max m) l_s (one pass over the 8 CTAs'
     // (m, l), kept in registers of the row's lane), then each output element is
     // sum_s w_s o_s[d] with the 8 remote loads independent of each other.
-    float* wts = part_l + kMaxRowTiles * 16;  // [rows per CTA][CS] local scratch
     const int n_my_rows = rows > rank ? (rows - rank + CS - 1) / CS : 0;
     if (threadIdx.x < n_my_rows) {
       const int r = rank + threadIdx.x * CS;
@@ -332,25 +401,36 @@ __global__ void __launch_bounds__((kMaxRowTiles + 1) * 32)
   cluster.sync();
 }
 
-template <int HD, int CS>
-cudaError_t launch_attention_hd(const CUtensorMap* tmK, const CUtensorMap* tmV, const AttnParams& p,
+template <int HD, int CS, int KG>
+cudaError_t launch_attention_kg(const CUtensorMap* tmK, const CUtensorMap* tmV, const AttnParams& p, int row_tiles,
                                 cudaStream_t st) {
   using C = AttnCfg<HD>;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e =
-        cudaFuncSetAttribute(attention_kernel<HD, CS>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(attention_kernel<HD, CS, KG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
     if (e == cudaSuccess && CS > 8)
-      e = cudaFuncSetAttribute(attention_kernel<HD, CS>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      e = cudaFuncSetAttribute(attention_kernel<HD, CS, KG>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
     configured = true;
   }
+  dim3 grid(CS, p.Hkv, p.B);
+  return launch_k_cluster(attention_kernel<HD, CS, KG>, grid, dim3((row_tiles * KG + 1) * 32), C::kSmemBytes, st,
+                          dim3(CS, 1, 1), *tmK, *tmV, p);
+}
+
+template <int HD, int CS>
+cudaError_t launch_attention_hd(const CUtensorMap* tmK, const CUtensorMap* tmV, const AttnParams& p,
+                                cudaStream_t st) {
   const int rows = p.W * (p.Hq / p.Hkv);
   const int row_tiles = (rows + 15) / 16;
   if (row_tiles > kMaxRowTiles) return cudaErrorInvalidValue;
-  dim3 grid(CS, p.Hkv, p.B);
-  return launch_k_cluster(attention_kernel<HD, CS>, grid, dim3((row_tiles + 1) * 32), C::kSmemBytes, st,
-                          dim3(CS, 1, 1), *tmK, *tmV, p);
+  const int pages_per_cta = ((p.kv_len_hint + kPage - 1) / kPage + CS - 1) / CS;
+  switch (key_groups(row_tiles, pages_per_cta)) {
+    case 4: return launch_attention_kg<HD, CS, 4>(tmK, tmV, p, row_tiles, st);
+    case 2: return launch_attention_kg<HD, CS, 2>(tmK, tmV, p, row_tiles, st);
+    default: return launch_attention_kg<HD, CS, 1>(tmK, tmV, p, row_tiles, st);
+  }
 }
 
 }  // namespace

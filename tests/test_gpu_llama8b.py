@@ -211,3 +211,41 @@ def test_repeated_scores_are_bit_identical(two_layer, B, W):
     first = m.score(ids, tok).clone()
     for _ in range(20):
         assert torch.equal(m.score(ids, tok), first)
+
+
+@pytest.fixture(scope="module")
+def two_layer_long():
+    need_gpu()
+    dims = synth.LLAMA8B.with_layers(2)
+    m = cuda_model(dims, {}, max_batch=2, max_width=16, max_seq_len=9300, num_pages=150)
+    m.load_weights(synth.iter_weights(dims, seed=4, device="cuda"))
+    yield dims, m
+    m.close()
+
+
+def test_long_cache_attention_paths_agree(two_layer_long):
+    """A 9000-token cache (141 pages, 9 per CTA): a width-8 window (two row tiles,
+    keys of each page split over two warps), eight decode steps (one row tile, four
+    key groups) and a width-16 window (four row tiles, no key split) score the same
+    positions alike."""
+    dims, m = two_layer_long
+    g = np.random.default_rng(9)
+    win = torch.from_numpy(g.integers(0, dims.vocab, (1, 16))).int().cuda()
+
+    def fresh():
+        m.seq_reset([0])
+        m.kv_fill_random([0], [9000], seed=12, scale=0.5)
+
+    fresh()
+    w8 = m.score([0], win[:, :8]).cpu().numpy()[0]
+    fresh()
+    w16 = m.score([0], win).cpu().numpy()[0]
+    fresh()
+    seq = []
+    for j in range(8):
+        m.decode_step([0], win[:, j])
+        seq.append(m.debug_logits(1).cpu().numpy()[0])
+    m.sync_status()
+    seq = np.stack(seq)
+    assert rel_err(w8, seq) < TOL
+    assert rel_err(w16[:8], w8) < TOL

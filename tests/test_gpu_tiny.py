@@ -308,3 +308,29 @@ def test_invalid_arguments(tiny):
     with pytest.raises(spec.SpecError) as e:
         m.sync_status()
     assert e.value.status == 1
+
+
+def test_long_context_attention_matches_oracle():
+    """A 4200-token cache: 66 pages per sequence, 5 per CTA of the 16-CTA cluster,
+    so the attention splits each page's keys over four warps and combines their
+    partials; logits of a verify window and of a decode step match the oracle."""
+    need_gpu()
+    w = synth.make_weights(synth.TINY, seed=8, gain_jitter=0.1)
+    kw = dict(max_batch=2, max_width=8, max_seq_len=4400, num_pages=80)
+    m = cuda_model(synth.TINY, w, **kw)
+    try:
+        g = np.random.default_rng(8)
+        prompt = g.integers(0, synth.TINY.vocab, 4200)
+        m.seq_reset([0])
+        m.prefill([0], torch.from_numpy(prompt[None]).int().cuda(), [4200])
+        o = oracle_for(synth.TINY, w, **kw)
+        o.prefill([0], [prompt])
+        win = np.concatenate([[prompt[-1]], g.integers(0, synth.TINY.vocab, 3)])[None]
+        got = m.score([0], torch.from_numpy(win).cuda()).cpu().numpy()
+        assert rel_err(got, o.forward([0], win)) < TOL
+        m.decode_step([0], torch.from_numpy(win[:, 0]).int().cuda())
+        got1 = m.debug_logits(1).cpu().numpy()
+        assert rel_err(got1, o.forward([0], win[:, :1])[:, 0]) < TOL
+        m.sync_status()
+    finally:
+        m.close()
