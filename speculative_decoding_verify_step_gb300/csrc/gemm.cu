@@ -61,6 +61,85 @@ SPEC_DEVICE_INLINE void named_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(N) : "memory");
 }
 
+// Rows [r_lo, r_hi) of the token tile that this CTA finishes: all of them, or with
+// split-K the share of split blockIdx.y.
+template <int ROWS>
+SPEC_DEVICE_INLINE void tile_rows(const EpiParams& p, int m0, int& r_lo, int& r_hi) {
+  r_lo = 0;
+  r_hi = min(ROWS, p.M - m0);
+  if (p.splits > 1) {
+    const int per = (ROWS + p.splits - 1) / p.splits;
+    r_lo = min(ROWS, (int)blockIdx.y * per);
+    r_hi = min(r_hi, r_lo + per);
+  }
+}
+
+// Epilogue inputs that do not depend on the mainloop (weight-row scales, the
+// input rows' sums of squares, the residual rows, RoPE angles, KV slots), loaded
+// into registers before it so that their latency hides behind the weight stream.
+// Token tiles of up to 16 rows only; wider tiles load them after the mainloop.
+template <int EPI, int NT, int ROWS>
+struct EpiPre {
+  static constexpr bool kOn = ROWS <= 16;
+  static constexpr int kWarps = NT / 32;
+  static constexpr int kRowsW = (ROWS + kWarps - 1) / kWarps;       // rows per warp (warp-per-row loops)
+  static constexpr int kPairs = (ROWS * (kBN / 2) + NT - 1) / NT;  // RoPE pairs per thread
+  float rs;                 // weight-row scale of column tid (tid < kBN)
+  float ssq[kRowsW][2];     // sum-of-squares tiles lane, lane + 32 of the warp's rows
+  float res[kRowsW][4];     // kEpiResid: residual at (row, column lane + 32 j)
+  float gn[4];              // kEpiResid: next gain of column lane + 32 j
+  int slot[kPairs];         // kEpiQKV: KV slot, cos, sin of each pair of this thread
+  float cs[kPairs], sn[kPairs];
+};
+
+template <int EPI, int NT, int ROWS>
+SPEC_DEVICE_INLINE void epi_prefetch(const EpiParams& p, EpiPre<EPI, NT, ROWS>& pre, int m0, int n0, int tid,
+                                     int warp, int lane) {
+  using E = EpiPre<EPI, NT, ROWS>;
+  if constexpr (E::kOn) {
+    int r_lo, r_hi;
+    tile_rows<ROWS>(p, m0, r_lo, r_hi);
+    pre.rs = tid < kBN ? __ldg(p.rscale + n0 + tid) : 0.f;
+#pragma unroll
+    for (int k = 0; k < E::kRowsW; ++k) {
+      const int r = r_lo + warp + k * E::kWarps;
+      pre.ssq[k][0] = pre.ssq[k][1] = 0.f;
+      if (r < r_hi && p.ssq_in) {
+        const int m = m0 + r;
+        if (lane < p.ssq_tiles) pre.ssq[k][0] = __ldcg(p.ssq_in + (long long)lane * p.ssq_stride + m);
+        if (lane + 32 < p.ssq_tiles) pre.ssq[k][1] = __ldcg(p.ssq_in + (long long)(lane + 32) * p.ssq_stride + m);
+      }
+      if constexpr (EPI == kEpiResid) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          pre.res[k][j] = r < r_hi ? __ldcg(p.resid + (long long)(m0 + r) * p.d + n0 + lane + 32 * j) : 0.f;
+      }
+    }
+    if constexpr (EPI == kEpiResid) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) pre.gn[j] = __ldg(p.g_next + n0 + lane + 32 * j);
+    }
+    if constexpr (EPI == kEpiQKV) {
+      const int half = p.hd >> 1;
+#pragma unroll
+      for (int k = 0; k < E::kPairs; ++k) {
+        const int e = tid + k * NT;
+        pre.slot[k] = -1;
+        pre.cs[k] = 1.f;
+        pre.sn[k] = 0.f;
+        if (e < max(0, r_hi - r_lo) * (kBN / 2)) {
+          const int m = m0 + r_lo + e / (kBN / 2), pr = e % (kBN / 2);
+          const int i = (n0 + (pr / half) * p.hd + pr % half) % p.hd;
+          const int pos = __ldcg(p.row_pos + m);
+          pre.slot[k] = __ldcg(p.row_slot + m);
+          pre.cs[k] = __ldg(p.rope_cos + (long long)pos * half + i);
+          pre.sn[k] = __ldg(p.rope_sin + (long long)pos * half + i);
+        }
+      }
+    }
+  }
+}
+
 // The end of a tile, common to both projection kernels.  Called by the NT
 // epilogue threads (tid 0..NT-1, warp = tid / 32) once this CTA's accumulator is
 // in `tile` (its own shared memory).  With split-K the splits of a tile form one
@@ -70,17 +149,16 @@ SPEC_DEVICE_INLINE void named_sync() {
 // the reduction is spread over the S CTAs and never leaves the chip.  The caller
 // holds back the CTA's exit with the matching cluster_wait().
 template <int EPI, int NT, int ROWS>
-SPEC_DEVICE_INLINE void finish_tile(const EpiParams& p, float* tile, float* s_scale, int m0, int n0, int tid,
-                                    int warp, int lane) {
+SPEC_DEVICE_INLINE void finish_tile(const EpiParams& p, const EpiPre<EPI, NT, ROWS>& pre, float* tile,
+                                    float* s_scale, int m0, int n0, int tid, int warp, int lane) {
+  using E = EpiPre<EPI, NT, ROWS>;
   constexpr int kGroupWarps = NT / 32;
-  int r_lo = 0, r_hi = min(ROWS, p.M - m0);
+  int r_lo, r_hi;
+  tile_rows<ROWS>(p, m0, r_lo, r_hi);
   if (p.splits > 1) {
     cluster_arrive();  // this CTA's partial tile is written
     cluster_wait();    // ... and every other split's
-    const int S = p.splits, rank = blockIdx.y;
-    const int per = (ROWS + S - 1) / S;
-    r_lo = min(ROWS, rank * per);
-    r_hi = min(r_hi, r_lo + per);
+    const int S = p.splits;
     for (int e = tid; e < max(0, r_hi - r_lo) * (kBN / 4); e += NT) {
       const int ml = r_lo + e / (kBN / 4), cl = (e % (kBN / 4)) * 4;
       const uint32_t off = smem_u32(tile + ml * kTilePad + cl);
@@ -103,28 +181,47 @@ SPEC_DEVICE_INLINE void finish_tile(const EpiParams& p, float* tile, float* s_sc
   }
   // weight-row scale 2^-e of the fp16 encoding, per output column of the tile
   __shared__ float s_rs[kBN];
-  for (int cl = tid; cl < kBN; cl += NT) s_rs[cl] = p.rscale[n0 + cl];
   // per-row scale of a normalised input: s_m = rsqrt(sum_t ssq[t][m] / d + eps).
-  // One warp per row, one tile partial per lane (independent loads, then a fixed
-  // shuffle tree: the same order on every run).
-#pragma unroll 4
-  for (int r = r_lo + warp; r < r_hi; r += kGroupWarps) {
-    const int m = m0 + r;
-    float sc = 1.f;
-    if (p.ssq_in) {
-      float ss = 0.f;
-      for (int t = lane; t < p.ssq_tiles; t += 32) ss += __ldcg(p.ssq_in + (long long)t * p.ssq_stride + m);
-      ss = warp_sum(ss);
-      sc = rsqrtf(ss * p.inv_d + p.eps);
+  // One warp per row, tiles lane, lane + 32, ... per lane (then a fixed shuffle
+  // tree: the same order on every run).
+  if constexpr (E::kOn) {
+    if (tid < kBN) s_rs[tid] = pre.rs;
+#pragma unroll
+    for (int k = 0; k < E::kRowsW; ++k) {
+      const int r = r_lo + warp + k * kGroupWarps;
+      if (r >= r_hi) break;
+      float sc = 1.f;
+      if (p.ssq_in) {
+        float ss = pre.ssq[k][0] + pre.ssq[k][1];
+        for (int t = lane + 64; t < p.ssq_tiles; t += 32) ss += __ldcg(p.ssq_in + (long long)t * p.ssq_stride + m0 + r);
+        ss = warp_sum(ss);
+        sc = rsqrtf(ss * p.inv_d + p.eps);
+      }
+      if (lane == 0) s_scale[r] = sc;
     }
-    if (lane == 0) s_scale[r] = sc;
+  } else {
+    for (int cl = tid; cl < kBN; cl += NT) s_rs[cl] = p.rscale[n0 + cl];
+#pragma unroll 4
+    for (int r = r_lo + warp; r < r_hi; r += kGroupWarps) {
+      const int m = m0 + r;
+      float sc = 1.f;
+      if (p.ssq_in) {
+        float ss = 0.f;
+        for (int t = lane; t < p.ssq_tiles; t += 32) ss += __ldcg(p.ssq_in + (long long)t * p.ssq_stride + m);
+        ss = warp_sum(ss);
+        sc = rsqrtf(ss * p.inv_d + p.eps);
+      }
+      if (lane == 0) s_scale[r] = sc;
+    }
   }
   named_sync<NT>();
 
   if constexpr (EPI == kEpiQKV) {
     // tile = 128 fused-QKV columns (one head of 128, or two of 64); RoPE pairs (i, i + hd/2)
     const int half = p.hd >> 1;
-    for (int e = tid; e < max(0, r_hi - r_lo) * (kBN / 2); e += NT) {
+#pragma unroll
+    for (int k = 0; k < (E::kOn ? E::kPairs : 1); ++k) {
+    for (int e = tid + k * NT; e < max(0, r_hi - r_lo) * (kBN / 2); e += (E::kOn ? E::kPairs : 1) * NT) {
       const int ml = r_lo + e / (kBN / 2), pr = e % (kBN / 2);
       const int m = m0 + ml;
       const int cl = (pr / half) * p.hd + pr % half;
@@ -134,9 +231,15 @@ SPEC_DEVICE_INLINE void finish_tile(const EpiParams& p, float* tile, float* s_sc
       float a = tile[ml * kTilePad + cl] * (sc * s_rs[cl]);
       float b = tile[ml * kTilePad + cl + half] * (sc * s_rs[cl + half]);
       if (head < p.Hq + p.Hkv) {
-        const int pos = p.row_pos[m];
-        const float cs = p.rope_cos[(long long)pos * half + i];
-        const float sn = p.rope_sin[(long long)pos * half + i];
+        float cs, sn;
+        if constexpr (E::kOn) {
+          cs = pre.cs[k];
+          sn = pre.sn[k];
+        } else {
+          const int pos = p.row_pos[m];
+          cs = p.rope_cos[(long long)pos * half + i];
+          sn = p.rope_sin[(long long)pos * half + i];
+        }
         const float ra = a * cs - b * sn;
         const float rb = a * sn + b * cs;
         a = ra;
@@ -147,7 +250,12 @@ SPEC_DEVICE_INLINE void finish_tile(const EpiParams& p, float* tile, float* s_sc
         q[i] = to_act(a);
         q[i + half] = to_act(b);
       } else {
-        const int slot = p.row_slot[m];
+        int slot;
+        if constexpr (E::kOn) {
+          slot = pre.slot[k];
+        } else {
+          slot = p.row_slot[m];
+        }
         if (slot < 0) continue;  // the round failed to get a page for this row
         const bool is_k = head < p.Hq + p.Hkv;
         const int kvh = is_k ? head - p.Hq : head - p.Hq - p.Hkv;
@@ -156,6 +264,7 @@ SPEC_DEVICE_INLINE void finish_tile(const EpiParams& p, float* tile, float* s_sc
         dst[i] = to_act(a);
         dst[i + half] = to_act(b);
       }
+    }
     }
   } else if constexpr (EPI == kEpiSwiGLU) {
     // tile = 64 gate rows then the 64 up rows of the same features
@@ -172,16 +281,27 @@ SPEC_DEVICE_INLINE void finish_tile(const EpiParams& p, float* tile, float* s_sc
   } else if constexpr (EPI == kEpiResid) {
     // r += y; next input X' = fp16(r * g_next); per-tile sum of r^2 for the next norm.
     // Warp w handles rows w, w+8, ...; lane covers columns lane + 32j (fixed order).
-    for (int ml = r_lo + warp; ml < r_hi; ml += kGroupWarps) {
+#pragma unroll
+    for (int k = 0; k < (E::kOn ? E::kRowsW : ROWS); ++k) {
+      const int ml = r_lo + warp + k * kGroupWarps;
+      if (ml >= r_hi) break;
       const int m = m0 + ml;
       float ss = 0.f;
 #pragma unroll
       for (int j = 0; j < kBN / 32; ++j) {
         const int cl = lane + 32 * j;
         const long long idx = (long long)m * p.d + n0 + cl;
-        const float r = p.resid[idx] + tile[ml * kTilePad + cl] * (s_scale[ml] * s_rs[cl]);
+        float rin, gn;
+        if constexpr (E::kOn) {
+          rin = pre.res[k][j];
+          gn = pre.gn[j];
+        } else {
+          rin = p.resid[idx];
+          gn = p.g_next[n0 + cl];
+        }
+        const float r = rin + tile[ml * kTilePad + cl] * (s_scale[ml] * s_rs[cl]);
         p.resid[idx] = r;
-        p.xn[idx] = to_act(r * p.g_next[n0 + cl]);
+        p.xn[idx] = to_act(r * gn);
         ss += r * r;
       }
       ss = warp_sum(ss);
@@ -300,6 +420,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   pdl_wait();
   pdl_launch_dependents();
   const int tid = threadIdx.x;  // 0..255
+  EpiPre<EPI, kConsumers, BM> pre;
+  epi_prefetch<EPI, kConsumers, BM>(p, pre, m0, n0, tid, warp, lane);
   float acc[BM / 8][4];
 #pragma unroll
   for (int t = 0; t < BM / 8; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
@@ -372,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     tile[(ml + 1) * kTilePad + wrow + g + 8] = acc[t][3];
   }
   named_sync<kConsumers>();
-  finish_tile<EPI, kConsumers, BM>(p, tile, s_scale, m0, n0, tid, warp, lane);
+  finish_tile<EPI, kConsumers, BM>(p, pre, tile, s_scale, m0, n0, tid, warp, lane);
   if (p.splits > 1) cluster_wait();  // the other splits are done reading this CTA's tile
 }
 
@@ -529,7 +651,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     return;
   }
   if (warp < 2) pdl_wait();  // outputs are written below by every warp
-  finish_tile<EPI, kTcThreads, NT>(p, reinterpret_cast<float*>(smem), s_scale, m0, n0, threadIdx.x, warp, lane);
+  EpiPre<EPI, kTcThreads, NT> pre;  // tiles of 128 or more rows load their epilogue inputs here
+  finish_tile<EPI, kTcThreads, NT>(p, pre, reinterpret_cast<float*>(smem), s_scale, m0, n0, threadIdx.x, warp,
+                                   lane);
   if (p.splits > 1) cluster_wait();  // the other splits are done reading this CTA's tile
 }
 
