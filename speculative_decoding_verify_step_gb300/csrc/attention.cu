@@ -36,6 +36,15 @@ namespace spec {
 
 namespace {
 
+// 2^x on the special-function unit (PTX ex2.approx, relative error about 2^-22;
+// subnormal results flush to zero).  The scores it exponentiates are rounded to
+// fp16 for the PV product, so the approximation is far below that rounding.
+SPEC_DEVICE_INLINE float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 constexpr int kAttnStages = 3;
 constexpr int kMaxRowTiles = 4;       // up to 64 query rows (W * group) per CTA
 constexpr int kMaxConsumerWarps = 4;  // row tiles x key groups
@@ -244,7 +253,7 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32)
         mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
         mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
         const float mnew = fmaxf(mrow[h], mx[h]);
-        alpha[h] = (mrow[h] == -INFINITY) ? 0.f : exp2f(mrow[h] - mnew);
+        alpha[h] = (mrow[h] == -INFINITY) ? 0.f : fast_exp2(mrow[h] - mnew);
         mrow[h] = mnew;
       }
       float rs[2] = {0.f, 0.f};
@@ -253,7 +262,7 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int h = e >> 1;
-          const float pv = (mrow[h] == -INFINITY) ? 0.f : exp2f(sc[t][e] - mrow[h]);
+          const float pv = (mrow[h] == -INFINITY) ? 0.f : fast_exp2(sc[t][e] - mrow[h]);
           sc[t][e] = pv;
           rs[h] += pv;
         }
@@ -331,7 +340,7 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32)
       float lt = 0.f;
 #pragma unroll
       for (int k = 0; k < KG; ++k) {
-        const float wk = (mt == -INFINITY || mk[k] == -INFINITY) ? 0.f : exp2f(mk[k] - mt);
+        const float wk = (mt == -INFINITY || mk[k] == -INFINITY) ? 0.f : fast_exp2(mk[k] - mt);
         kg_w[r * 4 + k] = wk;
         lt += wk * (k == 0 ? part_l[r] : kg_l[(t * (KG - 1) + k - 1) * 16 + rr]);
       }
@@ -375,7 +384,7 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32)
       float den = 0.f;
 #pragma unroll
       for (int s = 0; s < CS; ++s) {
-        ms[s] = (mmax == -INFINITY || ms[s] == -INFINITY) ? 0.f : exp2f(ms[s] - mmax);
+        ms[s] = (mmax == -INFINITY || ms[s] == -INFINITY) ? 0.f : fast_exp2(ms[s] - mmax);
         den += ms[s] * ls[s];
       }
       const float inv = den > 0.f ? 1.f / den : 0.f;
