@@ -408,6 +408,28 @@ class Bench:
                                     "frac_of_peak": round(by / (t / 1000) / 1e9 / hbm_peak, 4)}
         return out
 
+    def cost_curve(self, steps, warmup):
+        """Step time T(B, W) of this build's kernels over batch and verify width
+        ("投机解码的性能收支", section 四: the planner's cost table), prompt lengths
+        512..2048, and the width the planner picks from it for i.i.d. acceptance
+        alpha (largest accepted tokens per ms), with its alignment to the token tile."""
+        from speculative_decoding_verify_step_gb300 import planner
+        lens_all = self.synth.prompt_lengths(64, 512, 2048, seed=5).tolist()
+        widths = (1, 2, 3, 4, 5, 6, 8, 12, 16)
+        table, plan = {}, {}
+        for B in (1, 4, 16, 64):
+            row = {w: self.timed_rounds(B, w, lens_all[:B], steps, warmup) for w in widths}
+            table[str(B)] = {str(w): round(t, 4) for w, t in row.items()}
+            for alpha in (0.5, 0.7, 0.9):
+                surv = planner.survival_iid(alpha, 15)
+                best, theta = planner.choose_width(row, surv, B)
+                plan[f"B{B}_alpha{alpha}"] = {
+                    "width": best, "tok_per_ms": round(theta[best], 3),
+                    "speedup_vs_decode": round(theta[best] / theta[1], 3),
+                    "width_aligned_to_token_tile": planner.align_to_tile(best, B, 16)}
+        return {"step_ms": table, "planner": plan, "widths": list(widths),
+                "note": "rows per weight stream come in tiles of 8/16/32/64/128/256; T is nearly flat inside one"}
+
     def _barrier(self):
         torch = self.torch
         if torch.distributed.is_available() and torch.distributed.is_initialized():
@@ -689,6 +711,7 @@ def main():
             out["lam_sweep"] = lam_res
         if not args.no_configs:
             out["workloads"] = b.workloads(max(5, min(args.steps, 20)), 3, hbm_peak)
+            out["cost_curve"] = b.cost_curve(8, 2)
         if rank == 0 and not args.no_cpu_baseline:
             t_start = time.perf_counter()
             smp = OracleSample(args)
