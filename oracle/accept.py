@@ -301,3 +301,96 @@ def accept_tree_greedy(logits: np.ndarray, tok: np.ndarray, parent: np.ndarray):
         committed[b, k] = a
         bonus[b] = a
     return accepted, path, committed, bonus
+
+
+# ------------------------------------------------------------------ stochastic tree
+def residual_step(p_cur: np.ndarray, q_row: np.ndarray):
+    """One rejection of recursive rejection sampling over sibling candidates:
+    r = max(0, p - q) in float32, masses R = floor(r * 2^40), Z = sum R (exact), and
+    the normalised residual fl32(fl64(R) * fl64(1/Z)).  Z == 0 (no residual mass on
+    the grid, which exact arithmetic never reaches after a rejection) keeps p."""
+    r = residual(p_cur, q_row)
+    R = fixed_point_mass(r)
+    Z = int(np.sum(R, dtype=np.uint64))
+    if Z == 0:
+        return np.asarray(p_cur, np.float32).copy(), R
+    inv = np.float64(1.0) / np.float64(Z)
+    return (R.astype(np.float64) * inv).astype(np.float32), R
+
+
+def accept_tree_stochastic(p: np.ndarray, q, tok: np.ndarray, parent: np.ndarray, u: np.ndarray):
+    """Stochastic verification of a token tree (multi-draft speculative sampling).
+
+    Lecture 6 "Optimizing Autoregressive Decode" section 10.3: a tree of candidates
+    (SpecInfer, Miao et al. 2024) is verified in one forward under an ancestor mask;
+    "Per-step cost versus accepted tokens", section "Reefs": sampled (non-greedy)
+    tree verification exists beside the chain sampler.  The pages leave the rule
+    open; this is SpecInfer's multi-step speculative sampling, i.e. recursive
+    rejection sampling over the children of a node:
+
+    * at node v the target is p_cur = p[v]; the children c of v are tried in node
+      order: child c (token x) is accepted when fl32(u[c] * q_v(x)) < p_cur(x), and
+      the walk moves to c;
+    * after a rejection p_cur becomes the normalised residual max(0, p_cur - q_v)
+      (`residual_step`); after the last child is rejected the final token is drawn
+      from that residual (unnormalised masses, integer inverse CDF, u[0]);
+    * at a node without children the final (bonus) token is drawn from p[v] (u[0]).
+
+    q[b, v] is the distribution the children of node v were drawn from (i.i.d.);
+    q = None means deterministic candidates ("target only"): each child's q is the
+    one-hot of its own token, so a child is accepted with probability p_cur(x) and
+    a rejection removes x from the target.  With one child per node this is the
+    chain rule of `accept_stochastic` (tree u[c] = chain u[c-1], tree u[0] = chain
+    u[gamma]).
+
+    p [B, N, V] float32 (row c = target after node c), q [B, N, V] or None,
+    tok [B, N] (node 0 = pending token), parent [N] (BFS order), u [B, N] float32.
+    Returns (accepted [B], path [B, maxdepth] node ids (-1 padded),
+             committed [B, maxdepth+1] tokens (-1 padded), final [B]).
+    """
+    p = np.asarray(p, dtype=np.float32)
+    B, N, V = p.shape
+    parent = np.asarray(parent, dtype=np.int64)
+    depth = tree_depths(parent)
+    dmax = int(depth.max())
+    u = np.asarray(u, dtype=np.float32).reshape(B, N)
+    children = [[c for c in range(1, N) if parent[c] == v] for v in range(N)]
+    accepted = np.zeros(B, dtype=np.int64)
+    path = np.full((B, max(dmax, 1)), -1, dtype=np.int64)
+    committed = np.full((B, dmax + 1), -1, dtype=np.int64)
+    final = np.zeros(B, dtype=np.int64)
+    for b in range(B):
+        v, k = 0, 0
+        while True:
+            p_cur = p[b, v]
+            moved, R_last = -1, None
+            for j, c in enumerate(children[v]):
+                x = int(tok[b, c])
+                if q is None:
+                    q_row = np.zeros(V, np.float32)
+                    q_row[x] = 1.0
+                else:
+                    q_row = np.asarray(q[b, v], np.float32)
+                if accept_test(u[b, c:c + 1], q_row[x:x + 1], p_cur[x:x + 1])[0]:
+                    moved = c
+                    break
+                p_next, R_last = residual_step(p_cur, q_row)
+                if j == len(children[v]) - 1:
+                    break
+                p_cur = p_next
+            if moved >= 0:
+                path[b, k] = moved
+                committed[b, k] = int(tok[b, moved])
+                k += 1
+                v = moved
+                continue
+            if R_last is None:                       # no children: bonus from p at v
+                R_last = fixed_point_mass(p[b, v])
+            t = draw_index(R_last, float(u[b, 0]))
+            if t < 0:                                # residual without mass: draw from p_cur
+                t = draw_index(fixed_point_mass(p_cur), float(u[b, 0]))
+            final[b] = t
+            committed[b, k] = t
+            accepted[b] = k
+            break
+    return accepted, path, committed, final
