@@ -190,6 +190,31 @@ spec_status spec_verify_tree_step(spec_model* m, int32_t B, int32_t n_nodes, con
                                   const int32_t* tok, const int32_t* parent_host,
                                   int32_t* accepted, int32_t* committed, int32_t* bonus, void* stream);
 
+/* Sampled token-tree verify (multi-draft speculative sampling).  The pages name
+ * sampled tree verification (Lecture 6 section 10.3, SpecInfer; "Per-step cost
+ * versus accepted tokens", section "Reefs", the non-greedy tree sampler) without
+ * stating its rule; this is SpecInfer's multi-step speculative sampling, i.e.
+ * recursive rejection over the children of a node: from the root, the children c
+ * of the current node v are tried in node order; child c (token x) is accepted
+ * when fl32(u[b, c] * q_v(x)) < p_cur(x), where p_cur is the target at v (after
+ * temperature and top_k / top_p as in spec_verify_step) and, after each rejected
+ * child, the normalised residual max(0, p_cur - q_v) (masses floor(r * 2^40),
+ * p = fl32(fl64(R) * fl64(1 / sum R))).  After the last child of v is rejected
+ * the final token is drawn from that residual; at a node without children it is
+ * the bonus draw from the target at v; both by the integer inverse CDF with
+ * u[b, 0].  The output follows the target distribution when the children of node v
+ * were drawn i.i.d. from q[b, v] (q: device [B, n_nodes, vocab] fp32; rows of
+ * leaves unused) or, with q = NULL, for any fixed set of distinct candidate tokens
+ * (each child's q is then the one-hot of its own token).  u: device [B, n_nodes]
+ * fp32 in [0, 1).  With parent[c] = c - 1 this is spec_verify_step's rule (tree
+ * u[b, c] = chain u[b, c-1], tree u[b, 0] = chain u[b, gamma]).  Outputs and KV
+ * commit as spec_verify_tree_step.  temperature > 0. */
+spec_status spec_verify_tree_sampled(spec_model* m, int32_t B, int32_t n_nodes, const int32_t* seq_ids,
+                                     const int32_t* tok, const int32_t* parent_host, const float* q,
+                                     const float* u, float temperature, const int32_t* top_k,
+                                     const float* top_p, int32_t* accepted, int32_t* committed,
+                                     int32_t* bonus, void* stream);
+
 /* Forward only: score W rows per sequence (chain, or tree if parent_host != NULL)
  * and write the window's KV, without changing any committed length.  logits_out
  * (device [B, W, vocab] fp32) may be NULL. */
@@ -214,6 +239,14 @@ spec_status spec_accept_probs(int32_t B, int32_t gamma, int32_t V, const float* 
  * adjusted rows.  rows <= 65535, V <= 393216. */
 spec_status spec_adjust_probs(int32_t rows, int32_t V, const float* p, float* p_out, const int32_t* top_k,
                               const float* top_p, int32_t rows_per_setting, void* stream);
+
+/* Standalone sampled tree acceptance on given probabilities (no model): p [B, n_nodes,
+ * V] fp32 (row c = target after node c), q [B, n_nodes, V] or NULL, tok [B, n_nodes]
+ * (node 0 = pending token), parent_host HOST [n_nodes], u [B, n_nodes].  Same rule and
+ * outputs as spec_verify_tree_sampled, no KV commit; bit-exact by construction. */
+spec_status spec_accept_tree_probs(int32_t B, int32_t n_nodes, int32_t V, const float* p, const float* q,
+                                   const int32_t* tok, const int32_t* parent_host, const float* u,
+                                   int32_t* accepted, int32_t* committed, int32_t* bonus, void* stream);
 
 /* Standalone greedy acceptance on given logits [B, gamma+1, V] and drafts x [B, gamma]. */
 spec_status spec_accept_greedy(int32_t B, int32_t gamma, int32_t V, const float* logits, const int32_t* x,

@@ -389,6 +389,8 @@ def accept_tree_stochastic(p: np.ndarray, q, tok: np.ndarray, parent: np.ndarray
             t = draw_index(R_last, float(u[b, 0]))
             if t < 0:                                # residual without mass: draw from p_cur
                 t = draw_index(fixed_point_mass(p_cur), float(u[b, 0]))
+            if t < 0:                                # no mass at all (not a distribution): token 0
+                t = 0
             final[b] = t
             committed[b, k] = t
             accepted[b] = k

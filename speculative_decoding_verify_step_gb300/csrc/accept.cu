@@ -439,6 +439,48 @@ __global__ void __launch_bounds__(kAccThreads) accept_round_kernel(const __grid_
   }
 }
 
+// Commit an accepted tree path of sequence b (the whole block calls it): move the
+// path's KV (all layers, K and V) from slot L + node to slot L + depth, depth by
+// depth, then cut the cache to L + 1 + n and record the round's outputs.  The
+// destination L + d of depth d is never the source of a later depth (a node at
+// depth d' has index >= d' > d), but it can be the source of an earlier one, so the
+// depths run in order with a barrier between them.
+SPEC_DEVICE_INLINE void commit_tree_path(const TreeParams& p, int b, const int* path, int n, int tok_final) {
+  const int s = p.seq_ids[b];
+  const bool ok = s >= 0 && s < p.max_batch;  // a bad id was flagged by the prepare kernel
+  const int L = ok ? p.seq_len[s] : 0;
+  const int vec_per_head = p.hd / 8;  // 16-byte vectors
+  const int per_tok = p.n_layers * p.Hkv * vec_per_head;
+  for (int d = 1; d <= n && ok; ++d) {
+    const int src_t = L + path[d - 1], dst_t = L + d;
+    if (src_t / kPage < p.max_pages) {
+      const int src_pg = p.page_table[(long long)s * p.max_pages + src_t / kPage];
+      const int dst_pg = p.page_table[(long long)s * p.max_pages + dst_t / kPage];
+      if (src_pg >= 0 && dst_pg >= 0 && src_t != dst_t) {
+        for (int r = threadIdx.x; r < per_tok; r += blockDim.x) {
+          const int vec = r % vec_per_head;
+          const int kvh = (r / vec_per_head) % p.Hkv;
+          const int layer = r / (vec_per_head * p.Hkv);
+          const long long src =
+              ((((long long)layer * p.num_pages + src_pg) * p.Hkv + kvh) * kPage + src_t % kPage) * p.hd;
+          const long long dst =
+              ((((long long)layer * p.num_pages + dst_pg) * p.Hkv + kvh) * kPage + dst_t % kPage) * p.hd;
+          reinterpret_cast<uint4*>(p.kpool + dst)[vec] = reinterpret_cast<const uint4*>(p.kpool + src)[vec];
+          reinterpret_cast<uint4*>(p.vpool + dst)[vec] = reinterpret_cast<const uint4*>(p.vpool + src)[vec];
+        }
+      }
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    p.accepted[b] = n;
+    p.bonus[b] = tok_final;
+    if (ok)
+      truncate_seq(s, min(L + 1 + n, p.max_pages * kPage), p.seq_len, p.seq_npages, p.page_table, p.max_pages,
+                   p.free_bits);
+  }
+}
+
 __global__ void __launch_bounds__(kAccThreads) accept_tree_kernel(const __grid_constant__ TreeParams p) {
   __shared__ int s_path[kMaxWidth];
   __shared__ int s_n, s_tok;
@@ -476,36 +518,218 @@ __global__ void __launch_bounds__(kAccThreads) accept_tree_kernel(const __grid_c
   const int n = s_n;
   for (int j = threadIdx.x; j < N; j += kAccThreads)
     p.committed[row0 + j] = j < n ? p.tok[row0 + s_path[j]] : (j == n ? s_tok : -1);
-  const int s = p.seq_ids[b];
-  if (s < 0 || s >= p.max_batch) return;  // flagged by the prepare kernel
-  const int L = p.seq_len[s];
-  // Move the path's KV (all layers, K and V) from slot L + node to slot L + depth.
-  // Destination slots L+1..L+n never coincide with a later source slot (node >= depth).
-  const int vec_per_head = p.hd / 8;  // 16-byte vectors
-  const long long per_tok = (long long)p.n_layers * p.Hkv * vec_per_head;
-  for (long long e = threadIdx.x; e < per_tok * n; e += kAccThreads) {
-    const int d = (int)(e / per_tok) + 1;
-    const long long r = e % per_tok;
-    const int vec = (int)(r % vec_per_head);
-    const int kvh = (int)((r / vec_per_head) % p.Hkv);
-    const int layer = (int)(r / ((long long)vec_per_head * p.Hkv));
-    const int src_t = L + s_path[d - 1], dst_t = L + d;
-    if (src_t / kPage >= p.max_pages) continue;
-    const int src_pg = p.page_table[(long long)s * p.max_pages + src_t / kPage];
-    const int dst_pg = p.page_table[(long long)s * p.max_pages + dst_t / kPage];
-    if (src_pg < 0 || dst_pg < 0) continue;
-    const long long src = ((((long long)layer * p.num_pages + src_pg) * p.Hkv + kvh) * kPage + src_t % kPage) * p.hd;
-    const long long dst = ((((long long)layer * p.num_pages + dst_pg) * p.Hkv + kvh) * kPage + dst_t % kPage) * p.hd;
-    reinterpret_cast<uint4*>(p.kpool + dst)[vec] = reinterpret_cast<const uint4*>(p.kpool + src)[vec];
-    reinterpret_cast<uint4*>(p.vpool + dst)[vec] = reinterpret_cast<const uint4*>(p.vpool + src)[vec];
+  commit_tree_path(p, b, s_path, n, s_tok);
+}
+
+// Sum of a 64-bit per-thread value over the cluster: returns the total and, via
+// *before, the sum of the CTAs of lower rank plus this thread's exclusive prefix in
+// its CTA (thread order = vocabulary order).  Two cluster barriers.
+SPEC_DEVICE_INLINE unsigned long long cluster_scan_u64(cg::cluster_group& cluster, unsigned long long local,
+                                                       unsigned long long* s_scan, unsigned long long* s_total,
+                                                       unsigned long long* before) {
+  unsigned long long cta_total;
+  const unsigned long long pre = block_exscan_u64(local, s_scan, &cta_total);
+  if (threadIdx.x == 0) *s_total = cta_total;
+  cluster.sync();
+  const int rank = (int)cluster.block_rank();
+  unsigned long long S = 0, lower = 0;
+  for (int r = 0; r < (int)cluster.num_blocks(); ++r) {
+    const unsigned long long tr = *cluster.map_shared_rank(s_total, r);
+    if (r < rank) lower += tr;
+    S += tr;
+  }
+  cluster.sync();  // totals read before the next use may overwrite them
+  *before = lower + pre;
+  return S;
+}
+
+// Sampled verification of a token tree (SpecInfer's multi-step speculative
+// sampling = recursive rejection over the children of a node; Lecture 6
+// "Optimizing Autoregressive Decode" section 10.3).  From the root, the children of
+// the current node v are tried in node order: child c (token x) is accepted when
+// fl32(u[c] q_v(x)) < p_cur(x), where p_cur starts as the target at v and after
+// each rejection becomes the normalised residual max(0, p_cur - q) (masses
+// R = floor(r 2^40), p = fl32(fl64(R) * fl64(1/Z)), Z the exact sum); q_v is the
+// distribution the children were drawn from, or the one-hot of the child's own
+// token for deterministic candidates.  After the last child of v is rejected the
+// final token is drawn from that residual (integer inverse CDF with u[0]); at a
+// node without children it is the bonus draw from the target at v.  One cluster of
+// kDrawCluster CTAs per sequence splits the vocabulary for the residual sums and
+// the draw; every CTA takes the same decisions from the same values.
+template <PSource SRC>
+__global__ void __launch_bounds__(kAccThreads) accept_tree_sampled_kernel(const __grid_constant__ TreeParams p) {
+  __shared__ float s_max[kMaxWidth], s_z[kMaxWidth];
+  __shared__ int s_am[kMaxWidth];
+  __shared__ SelRow s_sel[kMaxWidth];
+  __shared__ double s_sinv[kMaxWidth];
+  __shared__ double s_rinv[kMaxWidth];  // 1/Z of each rejection at the current node (0: no mass, keep p)
+  __shared__ int s_rtok[kMaxWidth];     // deterministic candidates: the rejected tokens
+  __shared__ int s_path[kMaxWidth];
+  __shared__ int s_flag;
+  __shared__ unsigned long long s_scan[33], s_total;
+  pdl_wait();
+  pdl_launch_dependents();
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = (int)cluster.block_rank();
+  const int csize = (int)cluster.num_blocks();
+  const int b = blockIdx.y;
+  const int N = p.N, V = p.V;
+  const long long row0 = (long long)b * N;
+  const RoundAcceptParams& st = p.stats;
+  bool adjust = false;
+  if constexpr (SRC == PSource::kLogits) {
+    const int warp = threadIdx.x >> 5;
+    if (warp < N) merge_row_stats(st, row0 + warp, true, &s_max[warp], &s_z[warp], &s_am[warp]);
+    __syncthreads();
+    adjust = st.sel != nullptr;
+    if (adjust) {
+      if (threadIdx.x < N) {
+        const long long r = row0 + threadIdx.x;
+        s_max[threadIdx.x] = st.sel_max[r];
+        s_z[threadIdx.x] = st.sel_z[r];
+        s_sel[threadIdx.x] = st.sel[r];
+        s_sinv[threadIdx.x] = sel_inv_z(s_sel[threadIdx.x]);
+      }
+      __syncthreads();
+    }
+  }
+  auto base_prob = [&](int node, int w) -> float {
+    if constexpr (SRC == PSource::kProbs) {
+      return p.probs[(row0 + node) * V + w];
+    } else {
+      const float pv = prob_from_logit(st.logits[(row0 + node) * V + w], s_max[node], st.inv_temp, s_z[node]);
+      return adjust ? adjusted_prob(pv, w, s_sel[node], s_sinv[node]) : pv;
+    }
+  };
+  auto q_at = [&](int v, int j, int w) -> float {
+    return p.q ? p.q[(row0 + v) * V + w] : (w == s_rtok[j] ? 1.f : 0.f);
+  };
+  // the target at node v after r rejections, at token w
+  auto cur_prob = [&](int v, int r, int w) -> float {
+    float x = base_prob(v, w);
+    for (int j = 0; j < r; ++j) {
+      if (s_rinv[j] == 0.0) continue;
+      const float rr = fmaxf(0.f, __fsub_rn(x, q_at(v, j, w)));
+      x = __double2float_rn(__dmul_rn((double)grid_mass(rr), s_rinv[j]));
+    }
+    return x;
+  };
+  // this thread's contiguous vocabulary range
+  const int slice = (V + csize - 1) / csize;
+  const int s0 = min(V, rank * slice), s1 = min(V, s0 + slice);
+  const int chunk = (s1 - s0 + kAccThreads - 1) / kAccThreads;
+  const int v0 = min(s1, s0 + (int)threadIdx.x * chunk), v1 = min(s1, v0 + chunk);
+  const unsigned long long um = (unsigned long long)floorf(p.u[row0] * 16777216.0f);
+
+  int v = 0, k = 0;
+  while (true) {
+    int r = 0, moved = -1;
+    bool last_rejected = false;
+    int n_children = 0;
+    for (int c = 1; c < N; ++c) n_children += p.parent[c] == v;
+    int seen = 0;
+    for (int c = 1; c < N; ++c) {
+      if (p.parent[c] != v) continue;
+      ++seen;
+      const int x = p.tok[row0 + c];
+      if (threadIdx.x == 0) {
+        bool acc = false;
+        if (x < 0 || x >= V) {
+          if (rank == 0) set_status(st.status, SPEC_ERR_INVALID_ARG);
+        } else {
+          const float qx = p.q ? p.q[(row0 + v) * V + x] : 1.f;
+          acc = __fmul_rn(p.u[row0 + c], qx) < cur_prob(v, r, x);
+        }
+        s_flag = acc;
+        if (!acc && !p.q) s_rtok[r] = x;
+      }
+      __syncthreads();
+      if (s_flag) {
+        moved = c;
+        break;
+      }
+      if (seen == n_children) {
+        last_rejected = true;
+        break;
+      }
+      // normaliser of the residual after this rejection
+      unsigned long long local = 0;
+      for (int w = v0; w < v1; ++w) local += grid_mass(fmaxf(0.f, __fsub_rn(cur_prob(v, r, w), q_at(v, r, w))));
+      unsigned long long before;
+      const unsigned long long Z = cluster_scan_u64(cluster, local, s_scan, &s_total, &before);
+      if (threadIdx.x == 0) s_rinv[r] = Z ? __ddiv_rn(1.0, (double)Z) : 0.0;
+      __syncthreads();
+      ++r;
+    }
+    if (moved >= 0) {
+      if (threadIdx.x == 0) s_path[k] = moved;
+      __syncthreads();
+      ++k;
+      v = moved;
+      continue;
+    }
+    // final draw: the residual after the last rejection, or the target at a node
+    // without children; without mass on the grid, the current target
+    bool drawn = false;  // decided alike by every CTA (the totals are cluster-wide)
+    for (int pass = 0; pass < 2 && !drawn; ++pass) {
+      const bool resid = last_rejected && pass == 0;
+      if (pass == 1 && !last_rejected) break;
+      auto mass = [&](int w) -> unsigned long long {
+        const float pc = cur_prob(v, r, w);
+        return grid_mass(resid ? fmaxf(0.f, __fsub_rn(pc, q_at(v, r, w))) : pc);
+      };
+      unsigned long long local = 0;
+      for (int w = v0; w < v1; ++w) local += mass(w);
+      unsigned long long before;
+      const unsigned long long S = cluster_scan_u64(cluster, local, s_scan, &s_total, &before);
+      if (S == 0ull) continue;
+      // t = floor(m * S / 2^24) with a 128-bit product (m < 2^24, S < 2^58)
+      const unsigned long long hi = __umul64hi(um, S), lo = um * S;
+      const unsigned long long t = (hi << 40) | (lo >> 24);
+      drawn = true;  // the token is found by the thread whose range holds t
+      if (local > 0 && before <= t && t < before + local) {
+        unsigned long long run = before;
+        for (int w = v0; w < v1; ++w) {
+          run += mass(w);
+          if (run > t) {
+            s_flag = w;
+            break;
+          }
+        }
+        // this thread writes the round's outputs
+        for (int j = 0; j < N; ++j)
+          p.committed[row0 + j] = j < k ? p.tok[row0 + s_path[j]] : (j == k ? s_flag : -1);
+        if (p.path)
+          for (int j = 0; j < N; ++j) p.path[row0 + j] = j < k ? s_path[j] : -1;
+        p.accepted[b] = k;
+        p.bonus[b] = s_flag;
+      }
+    }
+    if (!drawn && rank == 0 && threadIdx.x == 0) {  // no mass anywhere: token 0
+      for (int j = 0; j < N; ++j) p.committed[row0 + j] = j < k ? p.tok[row0 + s_path[j]] : (j == k ? 0 : -1);
+      if (p.path)
+        for (int j = 0; j < N; ++j) p.path[row0 + j] = j < k ? s_path[j] : -1;
+      p.accepted[b] = k;
+      p.bonus[b] = 0;
+    }
+    break;
+  }
+}
+
+// KV commit of the sampled tree round (one block per sequence).
+__global__ void __launch_bounds__(kAccThreads) tree_commit_kernel(const __grid_constant__ TreeParams p) {
+  __shared__ int s_path[kMaxWidth];
+  __shared__ int s_n, s_tok;
+  pdl_wait();
+  pdl_launch_dependents();
+  const int b = blockIdx.x;
+  if (threadIdx.x < p.N) s_path[threadIdx.x] = p.path[(long long)b * p.N + threadIdx.x];
+  if (threadIdx.x == 0) {
+    s_n = p.accepted[b];
+    s_tok = p.bonus[b];
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    p.accepted[b] = n;
-    p.bonus[b] = s_tok;
-    truncate_seq(s, min(L + 1 + n, p.max_pages * kPage), p.seq_len, p.seq_npages, p.page_table, p.max_pages,
-                 p.free_bits);
-  }
+  commit_tree_path(p, b, s_path, s_n, s_tok);
 }
 
 }  // namespace
@@ -527,6 +751,18 @@ cudaError_t launch_accept_round(const RoundAcceptParams& p, bool sampled, cudaSt
   if (!sampled) return launch_k(accept_round_kernel<false>, dim3(1, p.B), dim3(kAccThreads), 0, st, p);
   return launch_k_cluster(accept_round_kernel<true>, dim3(kDrawCluster, p.B), dim3(kAccThreads), 0, st,
                           dim3(kDrawCluster, 1, 1), p);
+}
+
+cudaError_t launch_accept_tree_sampled(const TreeParams& p, cudaStream_t st) {
+  cudaError_t e;
+  if (p.probs)
+    e = launch_k_cluster(accept_tree_sampled_kernel<PSource::kProbs>, dim3(kDrawCluster, p.B), dim3(kAccThreads), 0,
+                         st, dim3(kDrawCluster, 1, 1), p);
+  else
+    e = launch_k_cluster(accept_tree_sampled_kernel<PSource::kLogits>, dim3(kDrawCluster, p.B), dim3(kAccThreads),
+                         0, st, dim3(kDrawCluster, 1, 1), p);
+  if (e != cudaSuccess || !p.path || !p.seq_ids) return e;
+  return launch_k(tree_commit_kernel, dim3(p.B), dim3(kAccThreads), 0, st, p);
 }
 
 cudaError_t launch_accept_tree(const TreeParams& p, cudaStream_t st) {

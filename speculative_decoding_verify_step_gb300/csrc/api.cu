@@ -119,6 +119,7 @@ struct spec_model {
   float *tstat_max = nullptr, *tstat_sum = nullptr;  // [V/128][M_max] LM-head tile statistics
   int32_t* tstat_arg = nullptr;
   SelRow* sel = nullptr;                  // [M_max] top-k / top-p kept set of each window row
+  int32_t* tree_path = nullptr;           // [M_max] accepted node ids of a sampled tree round
   float *sel_max = nullptr, *sel_z = nullptr;
   int32_t *row_pos = nullptr, *row_slot = nullptr, *seq_start = nullptr;
   int32_t *seq_wlen = nullptr, *seq_rowoff = nullptr;  // per-call window layout (prepare kernel)
@@ -550,6 +551,7 @@ spec_status spec_model_create(const spec_config* cfg, spec_model** out) {
   ALLOC(m->tstat_sum, (size_t)(V / 128) * M_max);
   ALLOC(m->tstat_arg, (size_t)(V / 128) * M_max);
   ALLOC(m->sel, M_max);
+  ALLOC(m->tree_path, M_max);
   ALLOC(m->sel_max, M_max);
   ALLOC(m->sel_z, M_max);
   ALLOC(m->row_pos, M_max);
@@ -776,6 +778,63 @@ spec_status spec_prefill(spec_model* m, int32_t B, const int32_t* seq_ids, const
   return SPEC_OK;
 }
 
+// Shared set-up of the tree acceptance parameters.
+TreeParams tree_params(spec_model* m, int B, int n_nodes, const int32_t* seq_ids, const int32_t* tok,
+                       const int32_t* parent_host, int32_t* accepted, int32_t* committed, int32_t* bonus) {
+  TreeParams tp{};
+  tp.B = B;
+  tp.N = n_nodes;
+  tp.V = m->cfg.vocab;
+  for (int j = 0; j < 16; ++j) tp.parent[j] = j < n_nodes ? parent_host[j] : -1;
+  tp.tok = tok;
+  tp.accepted = accepted;
+  tp.committed = committed;
+  tp.bonus = bonus;
+  tp.seq_ids = seq_ids;
+  tp.seq_len = m->seq_len;
+  tp.seq_npages = m->seq_npages;
+  tp.page_table = m->page_table;
+  tp.free_bits = m->free_bits;
+  tp.max_pages = m->max_pages;
+  tp.max_batch = m->cfg.max_batch;
+  tp.kpool = m->kpool;
+  tp.vpool = m->vpool;
+  tp.n_layers = m->cfg.n_layers;
+  tp.num_pages = m->cfg.num_pages;
+  tp.Hkv = m->cfg.n_kv_heads;
+  tp.hd = m->cfg.head_dim;
+  tp.status = m->status;
+  return tp;
+}
+
+spec_status spec_verify_tree_sampled(spec_model* m, int32_t B, int32_t n_nodes, const int32_t* seq_ids,
+                                     const int32_t* tok, const int32_t* parent_host, const float* q, const float* u,
+                                     float temperature, const int32_t* top_k, const float* top_p, int32_t* accepted,
+                                     int32_t* committed, int32_t* bonus, void* stream) {
+  if (spec_status s = check_model(m)) return s;
+  if (spec_status s = check_batch(m, B, n_nodes)) return s;
+  if (!seq_ids || !tok || !u || !accepted || !committed || !bonus) return fail(SPEC_ERR_INVALID_ARG, "NULL argument");
+  if (!(temperature > 0.f) || std::isinf(temperature))
+    return fail(SPEC_ERR_INVALID_ARG, "sampled tree verify needs temperature > 0");
+  int depth[16];
+  uint32_t anc[16];
+  if (auto s = tree_masks(n_nodes, parent_host, depth, anc)) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  g_launch_count = 0;
+  const float inv_t = 1.f / temperature;
+  if (auto s = forward(m, B, n_nodes, seq_ids, tok, depth, anc, true, true, inv_t, st)) return s;
+  TreeParams tp = tree_params(m, B, n_nodes, seq_ids, tok, parent_host, accepted, committed, bonus);
+  tp.stats = round_params(m, B, n_nodes - 1, seq_ids, tok, nullptr, u, inv_t, accepted, committed, bonus);
+  if (auto s = adjust_round(m, B, n_nodes, top_k, top_p, tp.stats, st)) return s;
+  tp.q = q;
+  tp.u = u;
+  tp.path = m->tree_path;
+  CUDA_TRY(launch_accept_tree_sampled(tp, st));
+  bump_bounds(m, n_nodes);
+  m->last_launches = g_launch_count;
+  return SPEC_OK;
+}
+
 spec_status spec_score(spec_model* m, int32_t B, int32_t W, const int32_t* seq_ids, const int32_t* tok,
                        const int32_t* parent_host, float* logits_out, void* stream) {
   if (spec_status s = check_model(m)) return s;
@@ -972,6 +1031,31 @@ spec_status spec_adjust_probs(int32_t rows, int32_t V, const float* p, float* p_
   sp.rows_per_set = rows_per_setting;
   sp.status = nullptr;
   CUDA_TRY(launch_select(sp, PSource::kProbs, rows, 1, static_cast<cudaStream_t>(stream)));
+  return SPEC_OK;
+}
+
+spec_status spec_accept_tree_probs(int32_t B, int32_t n_nodes, int32_t V, const float* p, const float* q,
+                                  const int32_t* tok, const int32_t* parent_host, const float* u, int32_t* accepted,
+                                  int32_t* committed, int32_t* bonus, void* stream) {
+  if (B < 1 || n_nodes < 1 || n_nodes > kMaxWidth || V < 1) return fail(SPEC_ERR_INVALID_ARG, "bad shape");
+  if (!p || !tok || !parent_host || !u || !accepted || !committed || !bonus)
+    return fail(SPEC_ERR_INVALID_ARG, "NULL argument");
+  int depth[16];
+  uint32_t anc[16];
+  if (auto s = tree_masks(n_nodes, parent_host, depth, anc)) return s;
+  TreeParams tp{};
+  tp.B = B;
+  tp.N = n_nodes;
+  tp.V = V;
+  for (int j = 0; j < 16; ++j) tp.parent[j] = j < n_nodes ? parent_host[j] : -1;
+  tp.tok = tok;
+  tp.accepted = accepted;
+  tp.committed = committed;
+  tp.bonus = bonus;
+  tp.q = q;
+  tp.u = u;
+  tp.probs = p;
+  CUDA_TRY(launch_accept_tree_sampled(tp, static_cast<cudaStream_t>(stream)));
   return SPEC_OK;
 }
 

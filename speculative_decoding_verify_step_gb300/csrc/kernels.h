@@ -223,8 +223,18 @@ struct TreeParams {
   __half* vpool;
   int n_layers, num_pages, Hkv, hd;
   int* status;
+  // sampled trees: q [B, N, V] (children of node v drawn i.i.d. from q[b, v]; null:
+  // deterministic candidates), u [B, N] (u[b, c] tests child c, u[b, 0] the final
+  // draw), probs [B, N, V] given probabilities (standalone; null: from the logits),
+  // path [B, N] accepted node ids for the commit (null: no commit)
+  const float* q;
+  const float* u;
+  const float* probs;
+  int32_t* path;
 };
 cudaError_t launch_accept_tree(const TreeParams& p, cudaStream_t st);
+// Sampled tree: the walk (cluster per sequence), then, if p.path and p.seq_ids, the KV commit.
+cudaError_t launch_accept_tree_sampled(const TreeParams& p, cudaStream_t st);
 
 struct ResetParams {
   const int32_t* seq_ids;

@@ -43,7 +43,7 @@ EXPORTS = ["spec_model_create", "spec_model_destroy", "spec_model_set_weight", "
            "spec_accept_greedy", "spec_get_kv_state", "spec_read_kv", "spec_debug_logits", "spec_kv_fill_random",
            "spec_sync_status", "spec_max_pages_per_seq", "spec_last_launch_count", "spec_last_error",
            "spec_set_profiling", "spec_read_profile", "spec_accept_greedy_noalloc", "spec_verify_ragged",
-           "spec_adjust_probs"]
+           "spec_adjust_probs", "spec_verify_tree_sampled", "spec_accept_tree_probs"]
 
 RAGGED_CAP_ACCEPT, RAGGED_COMPACT = 1, 2
 
@@ -73,6 +73,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "spec_verify_tree_step": (I32, [P, I32, I32, P, P, P, P, P, P, P]),
         "spec_verify_ragged": (I32, [P, I32, I32, P, P, P, I32, I32, P, P, F32, P, P, P, P, P, P]),
         "spec_adjust_probs": (I32, [I32, I32, P, P, P, P, I32, P]),
+        "spec_verify_tree_sampled": (I32, [P, I32, I32, P, P, P, P, P, F32, P, P, P, P, P, P]),
+        "spec_accept_tree_probs": (I32, [I32, I32, I32, P, P, P, P, P, P, P, P, P]),
         "spec_score": (I32, [P, I32, I32, P, P, P, P, P]),
         "spec_accept_probs": (I32, [I32, I32, I32, P, P, P, P, P, P, P, P]),
         "spec_accept_greedy": (I32, [I32, I32, I32, P, P, P, P, P, P]),
@@ -255,6 +257,25 @@ class SpecModel:
                                           _ptr(com), _ptr(bon), _stream()))
         return acc, com, bon
 
+    def verify_tree_sampled(self, seq_ids, tok, parent: Sequence[int], u, q=None, temperature: float = 1.0,
+                            outs=None, top_k=None, top_p=None):
+        """Sampled tree round: u [B, N]; q [B, N, V] (children of node v drawn from q[:, v])
+        or None (deterministic candidates).  Returns (accepted, committed [B, N], bonus)."""
+        sid = _dev_i32(seq_ids, self.device)
+        tk = _dev_i32(tok, self.device)
+        B, N = tk.shape
+        if outs is None:
+            outs = (torch.empty(B, dtype=torch.int32, device=self.device),
+                    torch.empty(B, N, dtype=torch.int32, device=self.device),
+                    torch.empty(B, dtype=torch.int32, device=self.device))
+        acc, com, bon = outs
+        kk, pp = _opt_dev(top_k, self.device, torch.int32), _opt_dev(top_p, self.device, torch.float32)
+        q, u = _f32(q), _f32(u)
+        _check(_lib.spec_verify_tree_sampled(self.handle, B, N, _ptr(sid), _ptr(tk), _i32_host(parent), _ptr(q),
+                                             _ptr(u), float(temperature), _ptr(kk), _ptr(pp), _ptr(acc), _ptr(com),
+                                             _ptr(bon), _stream()))
+        return acc, com, bon
+
     def score(self, seq_ids, tok, parent: Optional[Sequence[int]] = None, logits_out=None):
         sid = _dev_i32(seq_ids, self.device)
         tk = _dev_i32(tok, self.device)
@@ -341,6 +362,24 @@ def spec_adjust_probs(p: torch.Tensor, top_k=None, top_p=None, rows_per_setting:
     _check(lib.spec_adjust_probs(rows, V, _ptr(pp), _ptr(out), _ptr(kk), _ptr(tp), rows_per_setting, _stream()))
     torch.cuda.current_stream().synchronize()
     return out
+
+
+def spec_accept_tree_probs(p: torch.Tensor, q: Optional[torch.Tensor], tok, parent: Sequence[int], u: torch.Tensor):
+    """p [B, N, V], q [B, N, V] or None, tok [B, N], u [B, N] (CUDA).  Returns (accepted, committed, bonus)."""
+    lib = load_library()
+    B, N, V = p.shape
+    dev = p.device
+    acc = torch.empty(B, dtype=torch.int32, device=dev)
+    com = torch.empty(B, N, dtype=torch.int32, device=dev)
+    bon = torch.empty(B, dtype=torch.int32, device=dev)
+    tk = _dev_i32(tok, dev)
+    pp = p.float().contiguous()
+    qq = None if q is None else q.float().contiguous()
+    uu = u.float().contiguous()
+    _check(lib.spec_accept_tree_probs(B, N, V, _ptr(pp), _ptr(qq), _ptr(tk), _i32_host(parent), _ptr(uu), _ptr(acc),
+                                      _ptr(com), _ptr(bon), _stream()))
+    torch.cuda.current_stream().synchronize()
+    return acc, com, bon
 
 
 def spec_accept_greedy_noalloc(logits: torch.Tensor, x: Optional[torch.Tensor], outs=None):
