@@ -328,7 +328,7 @@ class Bench:
             res[W] = ms
         return {str(W): {"ms": round(ms, 4), "ratio_to_decode": round(ms / t_dec, 4)} for W, ms in res.items()}
 
-    def timed_rounds(self, B, W, lens, steps, warmup, tree=None, temp=1.0):
+    def timed_rounds(self, B, W, lens, steps, warmup, tree=None, temp=1.0, tree_sampled=False, top_p=None):
         """Mean ms of a round (W = 1: decode step) for B sequences whose caches hold
         `lens` tokens of random KV.  Sampled rounds use drafts that get rejected (q
         one-hot on a random token) so the cache grows one token per round; tree
@@ -344,7 +344,10 @@ class Bench:
         outs = (torch.empty(B, dtype=torch.int32, device=self.dev), torch.empty(B, W, dtype=torch.int32,
                                                                                 device=self.dev),
                 torch.empty(B, dtype=torch.int32, device=self.dev))
-        if tree is not None:
+        if tree is not None and tree_sampled:
+            u = torch.full((B, W), 0.5, device=self.dev)
+            run = lambda: self.model.verify_tree_sampled(dids, tok, tree, u, q=None, temperature=temp, outs=outs)
+        elif tree is not None:
             run = lambda: self.model.verify_tree_step(dids, tok, tree, outs=outs)
         elif W == 1:
             u = torch.full((B,), 0.5, device=self.dev)
@@ -353,7 +356,8 @@ class Bench:
             q = torch.zeros(B, W - 1, V, device=self.dev)
             q.scatter_(2, tok[:, 1:].long().unsqueeze(-1), 1.0)
             u = torch.full((B, W), 0.5, device=self.dev)
-            run = lambda: self.model.verify_step(dids, tok, q=q, u=u, temperature=temp, outs=outs)
+            tp = None if top_p is None else [top_p] * B
+            run = lambda: self.model.verify_step(dids, tok, q=q, u=u, temperature=temp, outs=outs, top_p=tp)
         for _ in range(warmup):
             run()
         torch.cuda.synchronize()
@@ -406,6 +410,14 @@ class Bench:
                                     "t_verify_over_t_decode": round(t / t_dec, 4), "rows": 60,
                                     "achieved_GBps": round(by / (t / 1000) / 1e9, 1),
                                     "frac_of_peak": round(by / (t / 1000) / 1e9 / hbm_peak, 4)}
+        ts = self.timed_rounds(4, len(tree), lens, steps, warmup, tree=tree, tree_sampled=True)
+        out["tree15_b4_ctx4096"]["sampled_verify_ms"] = round(ts, 4)
+        # sampling adjustments at the headline shape (the pages' sampled protocol: T = 1, top-p 0.95)
+        lens = [self.args.ctx] * 1
+        t0 = self.timed_rounds(1, 5, lens, steps, warmup)
+        t1 = self.timed_rounds(1, 5, lens, steps, warmup, top_p=0.95)
+        out["top_p095_b1_ctx1024_w5"] = {"verify_ms": round(t1, 4), "without_adjustment_ms": round(t0, 4),
+                                         "overhead_ms": round(t1 - t0, 4)}
         return out
 
     def cost_curve(self, steps, warmup):
