@@ -14,9 +14,10 @@
 // each, its probability keys held in shared memory).  Each threshold is found by
 // a most-significant-digit-first radix select over the 32-bit keys, 8 bits per
 // pass: every CTA builds a 256-bin histogram of counts and masses of its slice
-// (warp-aggregated shared-memory atomics: lanes with the same digit are merged
-// by __match_any_sync and summed with __reduce_add_sync first), the histograms
-// are added through distributed shared memory, and the bin where the running
+// with 32-bit shared-memory atomics (a mass, at most 2^40, is added as three
+// 32-bit parts that cannot overflow for a slice of probabilities; a warp whose
+// lanes share one digit adds once), the histograms are added through distributed
+// shared memory, and the bin where the running
 // count (top-k) or mass (top-p) from the top reaches the target fixes the next
 // 8 bits.  Equal keys at the final threshold are kept in index order: the CTA
 // holding the cut finds it with an ordered ballot scan and broadcasts it.
@@ -36,9 +37,12 @@ constexpr int kSelThreads = 512;
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kBins = 256;
 
+// A mass R <= 2^40 is accumulated as R[0:12) + R[12:26) << 12 + R[26:) << 26 in three
+// 32-bit counters: over at most 2^14 elements (a slice of a row) each part sums to
+// less than 2^28, and the native 32-bit shared atomics stay fast under conflicts.
 struct SelShared {
   unsigned int cnt[2][kBins];          // this CTA's histogram (double-buffered across passes)
-  unsigned long long mass[2][kBins];
+  unsigned int m0[2][kBins], m1[2][kBins], m2[2][kBins];
   unsigned int gc[kBins];              // cluster-wide histogram of the current pass
   unsigned long long gm[kBins];
   unsigned long long red[kSelWarps];
@@ -90,33 +94,48 @@ SPEC_DEVICE_INLINE SelectResult radix_select(cg::cluster_group& cluster, SelShar
   unsigned long long above_c = 0, above_m = 0;
   unsigned int tie_cnt = 0;
   bool ok = true;
-  const int iters = (n + kSelThreads - 1) / kSelThreads;
   for (int shift = 24; shift >= 0; shift -= 8) {
     const int buf = (pass++) & 1;
     for (int i = threadIdx.x; i < kBins; i += kSelThreads) {
       sh.cnt[buf][i] = 0;
-      sh.mass[buf][i] = 0;
+      sh.m0[buf][i] = sh.m1[buf][i] = sh.m2[buf][i] = 0;
     }
     __syncthreads();
-    for (int it = 0; it < iters; ++it) {  // warp-uniform trip count (match/reduce need whole warps)
-      const int i = it * kSelThreads + threadIdx.x;
-      uint32_t key = 0;
-      bool in = false;
-      if (i < n) {
-        key = keys[i];
-        in = (key & mask) == prefix;
-      }
+    // The leading digits of a probability row are concentrated in a few bins, so
+    // each thread sums a run of equal digits in registers and adds the run when
+    // the digit changes; at the end a warp whose lanes hold the same digit adds
+    // once.  (Spread digits add element by element.)
+    uint32_t cd = 0xffffffffu, cc = 0, c0 = 0, c1 = 0, c2 = 0;
+    auto flush = [&](uint32_t dd, uint32_t n_, uint32_t a0, uint32_t a1, uint32_t a2) {
+      atomicAdd(&sh.cnt[buf][dd], n_);
+      atomicAdd(&sh.m0[buf][dd], a0);
+      atomicAdd(&sh.m1[buf][dd], a1);
+      atomicAdd(&sh.m2[buf][dd], a2);
+    };
+    for (int i = threadIdx.x; i < n; i += kSelThreads) {
+      const uint32_t key = keys[i];
+      if ((key & mask) != prefix) continue;
       const uint32_t d = (key >> shift) & 0xffu;
-      const uint32_t peers = __match_any_sync(0xffffffffu, in ? d : 0xffffffffu);
-      if (in) {
-        const unsigned long long R = key_mass(key);  // <= 2^40: two 20-bit halves sum without overflow
-        const uint32_t lo = __reduce_add_sync(peers, (uint32_t)(R & 0xfffffu));
-        const uint32_t hi = __reduce_add_sync(peers, (uint32_t)(R >> 20));
-        if (lane == __ffs(peers) - 1) {
-          atomicAdd(&sh.cnt[buf][d], (unsigned int)__popc(peers));
-          atomicAdd(&sh.mass[buf][d], ((unsigned long long)hi << 20) + lo);
-        }
+      const unsigned long long R = key_mass(key);  // <= 2^40
+      if (d != cd) {
+        if (cc) flush(cd, cc, c0, c1, c2);
+        cd = d;
+        cc = c0 = c1 = c2 = 0;
       }
+      ++cc;
+      c0 += (uint32_t)(R & 0xfffu);
+      c1 += (uint32_t)((R >> 12) & 0x3fffu);
+      c2 += (uint32_t)(R >> 26);
+    }
+    const uint32_t cd0 = __shfl_sync(0xffffffffu, cd, 0);
+    if (__all_sync(0xffffffffu, cd == cd0)) {
+      cc = __reduce_add_sync(0xffffffffu, cc);
+      c0 = __reduce_add_sync(0xffffffffu, c0);
+      c1 = __reduce_add_sync(0xffffffffu, c1);
+      c2 = __reduce_add_sync(0xffffffffu, c2);
+      if (lane == 0 && cc) flush(cd0, cc, c0, c1, c2);
+    } else if (cc) {
+      flush(cd, cc, c0, c1, c2);
     }
     __syncthreads();
     cluster.sync();
@@ -126,7 +145,8 @@ SPEC_DEVICE_INLINE SelectResult radix_select(cg::cluster_group& cluster, SelShar
       for (int r = 0; r < csize; ++r) {
         const SelShared* rs = cluster.map_shared_rank(&sh, r);
         c += rs->cnt[buf][bin];
-        m += rs->mass[buf][bin];
+        m += (unsigned long long)rs->m0[buf][bin] + ((unsigned long long)rs->m1[buf][bin] << 12) +
+             ((unsigned long long)rs->m2[buf][bin] << 26);
       }
       sh.gc[bin] = c;
       sh.gm[bin] = m;
@@ -270,10 +290,23 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
 
   // probability keys of this CTA's slice, and the slice's mass
   unsigned long long local = 0;
-  for (int i = threadIdx.x; i < n; i += kSelThreads) {
-    const uint32_t key = prob_key(base_prob(s0 + i));
-    keys[i] = key;
-    local += key_mass(key);
+  constexpr int kUnroll = 8;  // independent loads in flight per thread
+  for (int i0 = threadIdx.x; i0 < n; i0 += kUnroll * kSelThreads) {
+    float pv[kUnroll];
+#pragma unroll
+    for (int j = 0; j < kUnroll; ++j) {
+      const int i = i0 + j * kSelThreads;
+      pv[j] = i < n ? base_prob(s0 + i) : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < kUnroll; ++j) {
+      const int i = i0 + j * kSelThreads;
+      if (i < n) {
+        const uint32_t key = prob_key(pv[j]);
+        keys[i] = key;
+        local += key_mass(key);
+      }
+    }
   }
   local = block_sum_u64(local, sh);
   if (threadIdx.x == 0) {
