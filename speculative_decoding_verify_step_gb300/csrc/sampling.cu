@@ -15,9 +15,10 @@
 // a most-significant-digit-first radix select over the 32-bit keys, 8 bits per
 // pass: every CTA builds a 256-bin histogram of counts and masses of its slice
 // with 32-bit shared-memory atomics (a mass, at most 2^40, is added as three
-// 32-bit parts that cannot overflow for a slice of probabilities; a warp whose
-// lanes share one digit adds once), the histograms are added through distributed
-// shared memory, and the bin where the running
+// 32-bit parts that cannot overflow for a slice of probabilities; each thread
+// first sums runs of equal digits in registers, and a warp whose lanes end on the
+// same digit adds once), the histograms are added through distributed shared
+// memory, and the bin where the running
 // count (top-k) or mass (top-p) from the top reaches the target fixes the next
 // 8 bits.  Equal keys at the final threshold are kept in index order: the CTA
 // holding the cut finds it with an ordered ballot scan and broadcasts it.
