@@ -20,7 +20,8 @@
 // in shared memory at the end.  Splitting the keys of a page over KG warps puts
 // a warp on every scheduler, so the short dependent MMA chains of a 16-row tile
 // overlap instead of running back to back.  A sequence's pages are split over a
-// thread-block cluster of 8 CTAs; each CTA leaves its partial (unnormalised O,
+// thread-block cluster of 1 to 16 CTAs (the widest whose grid fits one wave);
+// each CTA leaves its partial (unnormalised O,
 // running max, running sum) in its own shared memory and the cluster merges
 // them through distributed shared memory with log-sum-exp weights, so the
 // partials never go to HBM and no separate merge launch is needed.
@@ -446,11 +447,29 @@ cudaError_t launch_attention_hd(const CUtensorMap* tmK, const CUtensorMap* tmV, 
 
 cudaError_t launch_attention(const CUtensorMap* tmK, const CUtensorMap* tmV, const AttnParams& p, cudaStream_t st) {
   // 16-CTA clusters while they still fit in one wave (two CTAs per SM), else 8
-  const bool wide = p.B * p.Hkv * 16 <= 2 * p.sm_count;
-  if (p.hd == 128) return wide ? launch_attention_hd<128, 16>(tmK, tmV, p, st)
-                               : launch_attention_hd<128, 8>(tmK, tmV, p, st);
-  if (p.hd == 64) return wide ? launch_attention_hd<64, 16>(tmK, tmV, p, st)
-                              : launch_attention_hd<64, 8>(tmK, tmV, p, st);
+  // the widest cluster (16, 8, 4, 2 or 1 CTAs per sequence and kv head) whose grid
+  // still fits in one wave at two CTAs per SM: few sequences spread their pages over
+  // many SMs, many sequences keep more pages per CTA (and fewer merges)
+  int cs = 16;
+  while (cs > 1 && p.B * p.Hkv * cs > 2 * p.sm_count) cs >>= 1;
+  if (p.hd == 128) {
+    switch (cs) {
+      case 16: return launch_attention_hd<128, 16>(tmK, tmV, p, st);
+      case 8: return launch_attention_hd<128, 8>(tmK, tmV, p, st);
+      case 4: return launch_attention_hd<128, 4>(tmK, tmV, p, st);
+      case 2: return launch_attention_hd<128, 2>(tmK, tmV, p, st);
+      default: return launch_attention_hd<128, 1>(tmK, tmV, p, st);
+    }
+  }
+  if (p.hd == 64) {
+    switch (cs) {
+      case 16: return launch_attention_hd<64, 16>(tmK, tmV, p, st);
+      case 8: return launch_attention_hd<64, 8>(tmK, tmV, p, st);
+      case 4: return launch_attention_hd<64, 4>(tmK, tmV, p, st);
+      case 2: return launch_attention_hd<64, 2>(tmK, tmV, p, st);
+      default: return launch_attention_hd<64, 1>(tmK, tmV, p, st);
+    }
+  }
   return cudaErrorInvalidValue;
 }
 

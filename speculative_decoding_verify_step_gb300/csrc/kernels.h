@@ -81,7 +81,7 @@ struct AttnParams {
   int max_pages, max_batch;
   int B, W, Hq, Hkv, hd;       // W: the widest window of the call
   int layer_row0;              // first TMA row of this layer in the KV pool maps
-  int sm_count;                // picks the cluster size (8 or 16 CTAs per sequence and kv head)
+  int sm_count;                // picks the cluster size (1 to 16 CTAs per sequence and kv head)
   int kv_len_hint;             // upper bound of L + W over the batch (launch shape only)
   uint32_t anc[16];            // ancestor masks of the window rows (bit i: row i visible)
   __half* out;                 // [M, Hq*hd]

@@ -334,3 +334,33 @@ def test_long_context_attention_matches_oracle():
         m.sync_status()
     finally:
         m.close()
+
+
+def test_many_sequences_single_cta_attention():
+    """40 sequences x 4 kv heads leave one CTA per (sequence, kv head) in one wave
+    (no cluster merge): logits and the written KV still match the oracle."""
+    need_gpu()
+    w = synth.make_weights(synth.TINY, seed=9, gain_jitter=0.1)
+    B = 40
+    kw = dict(max_batch=B, max_width=4, max_seq_len=128, num_pages=2 * B + 8)
+    m = cuda_model(synth.TINY, w, **kw)
+    try:
+        g = np.random.default_rng(9)
+        lens = g.integers(5, 90, B)
+        prompts = [g.integers(0, synth.TINY.vocab, n) for n in lens]
+        ids = list(range(B))
+        m.seq_reset(ids)
+        tok = torch.zeros(B, int(lens.max()), dtype=torch.int32)
+        for b, pr in enumerate(prompts):
+            tok[b, :len(pr)] = torch.as_tensor(pr)
+        m.prefill(ids, tok.cuda(), lens.tolist())
+        o = oracle_for(synth.TINY, w, **kw)
+        o.prefill(ids, prompts)
+        win = np.concatenate([np.array([[pr[-1]] for pr in prompts]), g.integers(0, synth.TINY.vocab, (B, 2))], 1)
+        got = m.score(ids, torch.from_numpy(win).cuda()).cpu().numpy()
+        assert rel_err(got, o.forward(ids, win)) < TOL
+        lens_m, pt = m.kv_state(ids)
+        assert lens_m == o.lengths(ids).tolist()
+        m.sync_status()
+    finally:
+        m.close()
