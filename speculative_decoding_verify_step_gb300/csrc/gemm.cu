@@ -77,7 +77,8 @@ SPEC_DEVICE_INLINE void tile_rows(const EpiParams& p, int m0, int& r_lo, int& r_
 // Epilogue inputs that do not depend on the mainloop (weight-row scales, the
 // input rows' sums of squares, the residual rows, RoPE angles, KV slots), loaded
 // into registers before it so that their latency hides behind the weight stream.
-// Token tiles of up to 16 rows only; wider tiles load them after the mainloop.
+// Token tiles of up to 16 rows only (measured: for 32 rows the extra registers
+// spill, and wider tiles load them in the epilogue).
 template <int EPI, int NT, int ROWS>
 struct EpiPre {
   static constexpr bool kOn = ROWS <= 16;
@@ -500,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 
 // ----------------------------------------------------------------------------
-// tcgen05 path for more than 16 token rows: the same weight stream, but the
+// tcgen05 path from 64 token rows: the same weight stream, but the
 // contraction runs on the 5th-generation tensor cores.  One CTA = 128 weight
 // rows x NT token rows (NT in 32..256, so up to 256 rows stream each weight
 // tile exactly once).  Warp 0 drives TMA, one thread of warp 1 issues
@@ -651,7 +652,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     return;
   }
   if (warp < 2) pdl_wait();  // outputs are written below by every warp
-  EpiPre<EPI, kTcThreads, NT> pre;  // tiles of 128 or more rows load their epilogue inputs here
+  EpiPre<EPI, kTcThreads, NT> pre;  // loads its epilogue inputs row by row
   finish_tile<EPI, kTcThreads, NT>(p, pre, reinterpret_cast<float*>(smem), s_scale, m0, n0, threadIdx.x, warp,
                                    lane);
   if (p.splits > 1) cluster_wait();  // the other splits are done reading this CTA's tile
@@ -660,7 +661,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // Kernel, block size and dynamic shared memory of the projection for a token tile.
 template <int BM, int EPI>
 struct Kern {
-  static constexpr bool kTc = BM > 64;
+  static constexpr bool kTc = BM >= 64;  // tcgen05 from 64 token rows (measured: mma.sync is faster at 32)
   static auto fn() {
     if constexpr (kTc) {
       return gemm_tc_kernel<BM, EPI>;
@@ -737,7 +738,7 @@ int max_active_clusters_bm(int BM, int s) {
 template <int EPI>
 cudaError_t launch_epi(const CUtensorMap* tmW, const CUtensorMap* tmX, int BM, const EpiParams& p,
                        cudaStream_t st) {
-  switch (BM) {  // up to 64 token rows: mma.sync (HBM-bound); above: tcgen05
+  switch (BM) {  // up to 32 token rows: mma.sync (HBM-bound); from 64: tcgen05
     case 8: return launch_proj<8, EPI>(tmW, tmX, p, st);
     case 16: return launch_proj<16, EPI>(tmW, tmX, p, st);
     case 32: return launch_proj<32, EPI>(tmW, tmX, p, st);
