@@ -202,17 +202,23 @@ SPEC_DEVICE_INLINE void finish_tile(const EpiParams& p, const EpiPre<EPI, NT, RO
     }
   } else {
     for (int cl = tid; cl < kBN; cl += NT) s_rs[cl] = p.rscale[n0 + cl];
-#pragma unroll 4
-    for (int r = r_lo + warp; r < r_hi; r += kGroupWarps) {
-      const int m = m0 + r;
-      float sc = 1.f;
-      if (p.ssq_in) {
-        float ss = 0.f;
-        for (int t = lane; t < p.ssq_tiles; t += 32) ss += __ldcg(p.ssq_in + (long long)t * p.ssq_stride + m);
-        ss = warp_sum(ss);
-        sc = rsqrtf(ss * p.inv_d + p.eps);
+    // eight rows per warp at a time: their loads are issued together
+    for (int r0 = r_lo + warp; r0 < r_hi; r0 += 8 * kGroupWarps) {
+      float ss[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int r = r0 + j * kGroupWarps;
+        float a = 0.f;
+        if (r < r_hi && p.ssq_in)
+          for (int t = lane; t < p.ssq_tiles; t += 32) a += __ldcg(p.ssq_in + (long long)t * p.ssq_stride + m0 + r);
+        ss[j] = a;
       }
-      if (lane == 0) s_scale[r] = sc;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int r = r0 + j * kGroupWarps;
+        const float sum = warp_sum(ss[j]);
+        if (r < r_hi && lane == 0) s_scale[r] = p.ssq_in ? rsqrtf(sum * p.inv_d + p.eps) : 1.f;
+      }
     }
   }
   named_sync<NT>();
@@ -220,9 +226,8 @@ SPEC_DEVICE_INLINE void finish_tile(const EpiParams& p, const EpiPre<EPI, NT, RO
   if constexpr (EPI == kEpiQKV) {
     // tile = 128 fused-QKV columns (one head of 128, or two of 64); RoPE pairs (i, i + hd/2)
     const int half = p.hd >> 1;
-#pragma unroll
-    for (int k = 0; k < (E::kOn ? E::kPairs : 1); ++k) {
-    for (int e = tid + k * NT; e < max(0, r_hi - r_lo) * (kBN / 2); e += (E::kOn ? E::kPairs : 1) * NT) {
+    const int n_pairs = max(0, r_hi - r_lo) * (kBN / 2);
+    auto pair = [&](int e, float cs, float sn, int slot) {
       const int ml = r_lo + e / (kBN / 2), pr = e % (kBN / 2);
       const int m = m0 + ml;
       const int cl = (pr / half) * p.hd + pr % half;
@@ -232,15 +237,6 @@ SPEC_DEVICE_INLINE void finish_tile(const EpiParams& p, const EpiPre<EPI, NT, RO
       float a = tile[ml * kTilePad + cl] * (sc * s_rs[cl]);
       float b = tile[ml * kTilePad + cl + half] * (sc * s_rs[cl + half]);
       if (head < p.Hq + p.Hkv) {
-        float cs, sn;
-        if constexpr (E::kOn) {
-          cs = pre.cs[k];
-          sn = pre.sn[k];
-        } else {
-          const int pos = p.row_pos[m];
-          cs = p.rope_cos[(long long)pos * half + i];
-          sn = p.rope_sin[(long long)pos * half + i];
-        }
         const float ra = a * cs - b * sn;
         const float rb = a * sn + b * cs;
         a = ra;
@@ -250,14 +246,7 @@ SPEC_DEVICE_INLINE void finish_tile(const EpiParams& p, const EpiPre<EPI, NT, RO
         act_t* q = p.q_out + ((long long)m * p.Hq + head) * p.hd;
         q[i] = to_act(a);
         q[i + half] = to_act(b);
-      } else {
-        int slot;
-        if constexpr (E::kOn) {
-          slot = pre.slot[k];
-        } else {
-          slot = p.row_slot[m];
-        }
-        if (slot < 0) continue;  // the round failed to get a page for this row
+      } else if (slot >= 0) {  // slot < 0: the round failed to get a page for this row
         const bool is_k = head < p.Hq + p.Hkv;
         const int kvh = is_k ? head - p.Hq : head - p.Hq - p.Hkv;
         act_t* dst =
@@ -265,7 +254,38 @@ SPEC_DEVICE_INLINE void finish_tile(const EpiParams& p, const EpiPre<EPI, NT, RO
         dst[i] = to_act(a);
         dst[i + half] = to_act(b);
       }
-    }
+    };
+    if constexpr (E::kOn) {
+#pragma unroll
+      for (int k = 0; k < E::kPairs; ++k) {
+        const int e = tid + k * NT;
+        if (e < n_pairs) pair(e, pre.cs[k], pre.sn[k], pre.slot[k]);
+      }
+    } else {
+      // four pairs per thread at a time: positions and slots, then the angles, are
+      // loaded together before any of the four is written
+      constexpr int kB = 4;
+      for (int e0 = tid; e0 < n_pairs; e0 += kB * NT) {
+        int pos[kB], slot[kB];
+        float cs[kB], sn[kB];
+#pragma unroll
+        for (int j = 0; j < kB; ++j) {
+          const int e = e0 + j * NT;
+          const int m = m0 + r_lo + min(e, n_pairs - 1) / (kBN / 2);
+          pos[j] = p.row_pos[m];
+          slot[j] = p.row_slot[m];
+        }
+#pragma unroll
+        for (int j = 0; j < kB; ++j) {
+          const int pr = (e0 + j * NT) % (kBN / 2);
+          const int i = (n0 + (pr / half) * p.hd + pr % half) % p.hd;
+          cs[j] = p.rope_cos[(long long)pos[j] * half + i];
+          sn[j] = p.rope_sin[(long long)pos[j] * half + i];
+        }
+#pragma unroll
+        for (int j = 0; j < kB; ++j)
+          if (e0 + j * NT < n_pairs) pair(e0 + j * NT, cs[j], sn[j], slot[j]);
+      }
     }
   } else if constexpr (EPI == kEpiSwiGLU) {
     // tile = 64 gate rows then the 64 up rows of the same features
@@ -282,31 +302,46 @@ SPEC_DEVICE_INLINE void finish_tile(const EpiParams& p, const EpiPre<EPI, NT, RO
   } else if constexpr (EPI == kEpiResid) {
     // r += y; next input X' = fp16(r * g_next); per-tile sum of r^2 for the next norm.
     // Warp w handles rows w, w+8, ...; lane covers columns lane + 32j (fixed order).
-#pragma unroll
-    for (int k = 0; k < (E::kOn ? E::kRowsW : ROWS); ++k) {
-      const int ml = r_lo + warp + k * kGroupWarps;
-      if (ml >= r_hi) break;
+    auto row = [&](int ml, const float (&rin)[kBN / 32], const float (&gn)[kBN / 32]) {
       const int m = m0 + ml;
       float ss = 0.f;
 #pragma unroll
       for (int j = 0; j < kBN / 32; ++j) {
         const int cl = lane + 32 * j;
         const long long idx = (long long)m * p.d + n0 + cl;
-        float rin, gn;
-        if constexpr (E::kOn) {
-          rin = pre.res[k][j];
-          gn = pre.gn[j];
-        } else {
-          rin = p.resid[idx];
-          gn = p.g_next[n0 + cl];
-        }
-        const float r = rin + tile[ml * kTilePad + cl] * (s_scale[ml] * s_rs[cl]);
+        const float r = rin[j] + tile[ml * kTilePad + cl] * (s_scale[ml] * s_rs[cl]);
         p.resid[idx] = r;
-        p.xn[idx] = to_act(r * gn);
+        p.xn[idx] = to_act(r * gn[j]);
         ss += r * r;
       }
       ss = warp_sum(ss);
       if (lane == 0) p.ssq_out[(long long)(n0 / kBN) * p.ssq_stride + m] = ss;
+    };
+    if constexpr (E::kOn) {
+#pragma unroll
+      for (int k = 0; k < E::kRowsW; ++k) {
+        const int ml = r_lo + warp + k * kGroupWarps;
+        if (ml >= r_hi) break;
+        row(ml, pre.res[k], pre.gn);
+      }
+    } else {
+      float gn[kBN / 32];
+#pragma unroll
+      for (int j = 0; j < kBN / 32; ++j) gn[j] = p.g_next[n0 + lane + 32 * j];
+      // four rows per warp at a time: their residuals are loaded before any is written
+      constexpr int kB = 4;
+      for (int r0 = r_lo + warp; r0 < r_hi; r0 += kB * kGroupWarps) {
+        float rin[kB][kBN / 32];
+#pragma unroll
+        for (int k = 0; k < kB; ++k) {
+          const int ml = min(r0 + k * kGroupWarps, r_hi - 1);
+#pragma unroll
+          for (int j = 0; j < kBN / 32; ++j) rin[k][j] = p.resid[(long long)(m0 + ml) * p.d + n0 + lane + 32 * j];
+        }
+#pragma unroll
+        for (int k = 0; k < kB; ++k)
+          if (r0 + k * kGroupWarps < r_hi) row(r0 + k * kGroupWarps, rin[k], gn);
+      }
     }
   } else {  // kEpiLogits: logits = s_m * y, plus per-tile softmax statistics of each row
     for (int ml = r_lo + warp; ml < r_hi; ml += kGroupWarps) {
