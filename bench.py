@@ -160,6 +160,7 @@ class Bench:
         self.ids = torch.arange(B, dtype=torch.int32, device=device)
         self.prompts = synth.prompts(B, ctx + 1, self.dims.vocab, seed=2).to(device)
         self.stream = torch.cuda.current_stream()
+        self.tensor_peak = measured_peaks()[1]
 
     def reset(self):
         B = self.B
@@ -225,6 +226,58 @@ class Bench:
         self._barrier()
         self.model.sync_status()
         return e0.elapsed_time(e1), acc_log.cpu(), launches, clocks
+
+    def round_distribution(self, rounds, warmup, temp):
+        """Per-round device time of the recorded rounds (an event pair around each
+        round on the launch stream): median, 20th and 80th percentile in ms."""
+        torch = self.torch
+        self.reset()
+        outs = None
+        evs = []
+        for r, (tok, q, u) in enumerate(rounds):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            outs = self.model.verify_step(self.ids, tok, q=q, u=u, temperature=temp, outs=outs)
+            e1.record()
+            if r >= warmup:
+                evs.append((e0, e1))
+        torch.cuda.synchronize()
+        t = sorted(a.elapsed_time(b) for a, b in evs)
+        pick = lambda f: round(t[min(len(t) - 1, int(f * len(t)))], 5)
+        return {"median": pick(0.5), "p20": pick(0.2), "p80": pick(0.8), "rounds": len(t)}
+
+    def graph_round(self, rounds, temp, reps=50):
+        """One recorded round captured as a CUDA graph (programmatic launch edges
+        included) and replayed: device ms per replay.  Replays repeat the same
+        inputs, so the cache grows by the round's commit each time."""
+        torch = self.torch
+        self.reset()
+        tok, q, u = rounds[0]
+        outs = (torch.empty(self.B, dtype=torch.int32, device=self.dev),
+                torch.empty(self.B, tok.shape[1], dtype=torch.int32, device=self.dev),
+                torch.empty(self.B, dtype=torch.int32, device=self.dev))
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                self.model.verify_step(self.ids, tok, q=q, u=u, temperature=temp, outs=outs)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.model.verify_step(self.ids, tok, q=q, u=u, temperature=temp, outs=outs)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        self.model.sync_status()
+        return e0.elapsed_time(e1) / reps
 
     def replay_e2e(self, rounds, warmup, temp):
         """Same rounds, inputs from pinned host memory and outputs read back every step."""
@@ -383,11 +436,15 @@ class Bench:
             t_dec = self.timed_rounds(B, 1, lens, steps, warmup)
             t_ver = self.timed_rounds(B, 5, lens, steps, warmup)
             by = wb + kv_tok * (sum(lens) + 5 * B)
+            d = self.dims
+            flops = 2.0 * (wb / 2.0) * 5 * B + 4.0 * d.n_heads * d.head_dim * d.n_layers * 5 * (sum(lens) + 5 * B)
             sweep[str(B)] = {"verify_ms": round(t_ver, 4), "decode_ms": round(t_dec, 4),
                              "t_verify_over_t_decode": round(t_ver / t_dec, 4),
                              "rows": 5 * B, "algorithmic_GB": round(by / 1e9, 3),
                              "achieved_GBps": round(by / (t_ver / 1000) / 1e9, 1),
-                             "frac_of_peak": round(by / (t_ver / 1000) / 1e9 / hbm_peak, 4)}
+                             "frac_of_peak": round(by / (t_ver / 1000) / 1e9 / hbm_peak, 4),
+                             "achieved_TFLOPs": round(flops / (t_ver / 1000) / 1e12, 2),
+                             "frac_of_tensor_peak": round(flops / (t_ver / 1000) / 1e12 / self.tensor_peak, 4)}
         out["batch_sweep_w5_ctx512_2048"] = sweep
         lc = {}
         lens = [32768] * 8
@@ -548,6 +605,44 @@ class OracleSample:
                 f"(lam={a.lam}); per-layer time x 32 layers")
 
 
+def oracle_tiny_rounds_per_s(n_rounds=8):
+    """The oracle on the tiny configuration (2 layers, d 256, vocab 1024, B = 2,
+    64-token prompts, gamma = 3, sampled, lam = 0.5): full rounds per second."""
+    import time as _t
+
+    import numpy as np
+
+    from oracle import accept as A
+    from oracle.decoder import OracleDecoder, weights_to_numpy
+    from speculative_decoding_verify_step_gb300 import synth
+    dims = synth.TINY
+    o = OracleDecoder(dims, weights_to_numpy(synth.make_weights(dims, seed=1)), max_batch=2, max_seq_len=256,
+                      num_pages=8)
+    g = np.random.default_rng(2)
+    prompts = [g.integers(0, dims.vocab, 64) for _ in range(2)]
+    o.prefill([0, 1], prompts)
+    pending = np.array([pr[-1] for pr in prompts])
+    gamma, V = 3, dims.vocab
+    t0 = _t.perf_counter()
+    for r in range(n_rounds):
+        tok = np.zeros((2, gamma + 1), np.int64)
+        tok[:, 0] = pending
+        q = np.zeros((2, gamma, V), np.float32)
+        D = synth.dirichlet1((2, gamma, V), seed=r).numpy()
+        for i in range(gamma):
+            pi = A.target_probs(o.forward([0, 1], tok[:, :i + 1])[:, i], 1.0).astype(np.float64)
+            q[:, i] = (0.5 * pi + 0.5 * D[:, i]).astype(np.float32)
+            for b in range(2):
+                c = np.cumsum(q[b, i].astype(np.float64))
+                tok[b, i + 1] = min(int(np.searchsorted(c, g.random() * c[-1], side="right")), V - 1)
+        u = synth.uniforms((2, gamma + 1), seed=100 + r).numpy()
+        p = A.target_probs(o.forward([0, 1], tok), 1.0)
+        n, com, bon, _ = A.accept_stochastic(p, q, tok[:, 1:], u)
+        o.commit([0, 1], n, gamma + 1)
+        pending = bon
+    return n_rounds / (_t.perf_counter() - t0)
+
+
 def cpu_threads():
     try:
         from threadpoolctl import threadpool_info
@@ -695,6 +790,7 @@ def main():
         out["step_roofline"] = {"algorithmic_bytes": wb + kvb, "achieved_GBps": round((wb + kvb) / (ms_per_step / 1000)
                                                                                   / 1e9, 1),
                                 "frac_of_peak": round((wb + kvb) / (ms_per_step / 1000) / 1e9 / hbm_peak, 4),
+                                "frac_of_8TBps_nominal": round((wb + kvb) / (ms_per_step / 1000) / 8e12, 4),
                                 "ideal_ms_at_peak": round((wb + kvb) / (hbm_peak * 1e9) * 1000, 4)}
         if not args.no_e2e:
             e_ms, e_acc, h2d, d2h = b.replay_e2e(rounds, args.warmup, temp)
@@ -708,9 +804,21 @@ def main():
                 e_ms, e_tokens = float(mx[0]), float(sm[1])
             out["e2e"] = {"value": round(e_tokens / (e_ms / 1000), 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                           "d2h_bytes_per_step": d2h, "ms_per_step": round(e_ms / args.steps, 5)}
+        out["round_ms"] = b.round_distribution(rounds, args.warmup, temp)
+        try:
+            out["graph_round_ms"] = round(b.graph_round(rounds, temp), 5)
+        except Exception as exc:  # capture not possible on this torch build: say so
+            out["graph_round_ms"] = None
+            out["graph_round_error"] = str(exc)[:200]
         if not args.no_sweep:
             sw_steps = max(10, min(args.steps, 50))
             out["t_verify_over_t_decode"] = b.width_sweep(range(1, 9), sw_steps, 3)
+            # "Per-step cost versus accepted tokens" section 2: speedup = tokens per round x
+            # T_decode / (T_verify + T_draft), with a draft costing c decode steps per guess
+            sw = out["t_verify_over_t_decode"]
+            t_dec, t_ver = sw["1"]["ms"], sw[str(gamma + 1)]["ms"]
+            out["speedup_projection"] = {f"c={c}": round(mean_tpr * t_dec / (t_ver + gamma * c * t_dec), 3)
+                                         for c in (0.0, 0.05, 0.19)}
         if not args.no_lam_sweep:
             lam_res = {}
             for lm in (0.2, 0.5, 0.8):
@@ -736,6 +844,7 @@ def main():
                 raw += r
                 n += 1
             out["cpu_baseline"] = {"value": round(toks / secs, 5), "unit": UNIT, "cores": cpu_threads(),
+                                   "tiny_config_rounds_per_s": round(oracle_tiny_rounds_per_s(), 2),
                                    "kind": "oracle",
                                    "sample": smp.describe() + f"; {n} rounds, {raw / n:.2f} s measured per "
                                              f"sample round, {secs / n:.2f} s scaled"}
