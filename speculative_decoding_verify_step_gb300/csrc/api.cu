@@ -177,6 +177,9 @@ spec_status validate_cfg(const spec_config& c) {
   return SPEC_OK;
 }
 
+// Bytes HBM moves during a latency-bound attention launch (~10 us at ~6.5 TB/s).
+constexpr double kAttnL2Budget = 64e6;
+
 long long max_len_bound(const spec_model* m) {
   long long b = 0;
   for (long long v : m->host_len_bound) b = std::max(b, v);
@@ -264,8 +267,19 @@ spec_status forward(spec_model* m, int B, int W, const int32_t* seq_ids, const i
   // K/V bytes of one attention launch: the host-side bound on the cached lengths
   const long long bound = std::min<long long>(max_len_bound(m) + W, c.max_seq_len);
   const double kv_bytes = 2.0 * 2.0 * hd * Hkv * (double)B * (double)bound;
+  // While a short-context attention runs, HBM has room for about kAttnL2Budget
+  // bytes beyond the attention's own K/V: that much of the O projection's and
+  // then the gate/up projection's weights is prefetched into L2 (none once the
+  // K/V reads alone fill the attention's time).
+  const double pf = std::max(0.0, kAttnL2Budget - kv_bytes);
+  const unsigned long long pf_o = (unsigned long long)std::min(pf, wb_o) & ~15ull;
+  const unsigned long long pf_gu = (unsigned long long)std::max(0.0, std::min(pf - (double)pf_o, wb_gu)) & ~15ull;
   for (int l = 0; l < c.n_layers; ++l) {
     auto& Ly = m->layers[l];
+    ap.l2_next[0] = Ly.wo;
+    ap.l2_next_bytes[0] = pf_o;
+    ap.l2_next[1] = Ly.wgu;
+    ap.l2_next_bytes[1] = pf_gu;
     {
       EpiParams e = base;
       e.N = m->qkv_n;

@@ -79,6 +79,9 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kAttnStages * C::kStageBytes);
   uint64_t* empty = full + kAttnStages;
   __shared__ int s_fail;
+  // ancestor masks in shared memory: read with a per-row index, which from the
+  // parameter bank would be a divergent constant load repeated for every page
+  __shared__ uint32_t s_anc[16];
   cg::cluster_group cluster = cg::this_cluster();
 
   const int rank = (int)cluster.block_rank();  // == blockIdx.x: the split of this CTA
@@ -118,20 +121,20 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32)
     s_fail = 0;
     fence_barrier_init();
   }
+  if (threadIdx.x < 16) s_anc[threadIdx.x] = p.anc[threadIdx.x];
   __syncthreads();
 
   // partials of this CTA, reusing the stage buffers once the pipeline is drained
   float* part_o = reinterpret_cast<float*>(smem);            // [rows][HD]
   float* part_m = part_o + kMaxRowTiles * 16 * HD;           // [rows]
   float* part_l = part_m + kMaxRowTiles * 16;                // [rows]
-  float* wts = part_l + kMaxRowTiles * 16;                   // [rows per CTA][CS] merge weights
-  float* kg_o = wts + kMaxRowTiles * 16 * 16;                // [slots][16][HD] key-group partials
+  float* kg_o = part_l + kMaxRowTiles * 16;                  // [slots][16][HD] key-group partials
   float* kg_m = kg_o + kMaxKgSlots * 16 * HD;                // [slots][16]
   float* kg_l = kg_m + kMaxKgSlots * 16;
   float* kg_w = kg_l + kMaxKgSlots * 16;                     // [rows][KG] combine weights
   float* cm = kg_w + kMaxRowTiles * 16 * 4;                  // [rows] combined max, sum
   float* cl = cm + kMaxRowTiles * 16;
-  static_assert((kMaxRowTiles * 16 * (HD + 2 + 16 + 4 + 2) + kMaxKgSlots * 16 * (HD + 2)) * 4 <=
+  static_assert((kMaxRowTiles * 16 * (HD + 2 + 4 + 2) + kMaxKgSlots * 16 * (HD + 2)) * 4 <=
                     kAttnStages * 2 * kPage * HD * 2,
                 "partials fit in the stage buffers");
 
@@ -169,6 +172,10 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32)
   } else {
     // ---------------------------------------------------------------- consumers
     pdl_wait();  // q is written by the QKV projection
+    if (warp == 0 && lane == 0) {
+      l2_prefetch_share(p.l2_next[0], p.l2_next_bytes[0]);
+      l2_prefetch_share(p.l2_next[1], p.l2_next_bytes[1]);
+    }
     const int g = lane >> 2, c = lane & 3;
     const int rt = warp / KG, kg = warp % KG;  // row tile, key group (keys kg*16*KT .. of each page)
     // query rows of this thread: r0 = rt*16 + g, r1 = r0 + 8; row r -> window row j = r / grp
@@ -195,8 +202,8 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32)
         qa[ks][2 + h] = hi;   // a4a5 / a6a7
       }
     }
-    const uint32_t anc0 = valid[0] ? p.anc[jrow[0]] : 0u;
-    const uint32_t anc1 = valid[1] ? p.anc[jrow[1]] : 0u;
+    const uint32_t anc0 = valid[0] ? s_anc[jrow[0]] : 0u;
+    const uint32_t anc1 = valid[1] ? s_anc[jrow[1]] : 0u;
     const float scale_log2 = 1.4426950408889634f / sqrtf((float)HD);
 
     float acc[HD / 8][4];
@@ -234,16 +241,37 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32)
       // mask + online softmax (exp2 domain)
       const int key0 = (pg0 + i) * kPage + kg * KT * 16;
       float mx[2] = {-INFINITY, -INFINITY};
+      // visibility of the page's 64 keys for this thread's two rows (bit k: key
+      // key0p + k), then of this thread's keys of the slice (bit t*2 + (e&1))
+      uint32_t vb[2];
+      {
+        const int key0p = (pg0 + i) * kPage;
+        const int hist = min(max(L - key0p, 0), kPage);  // cached keys at the page start
+        const uint64_t hmask = hist == kPage ? ~0ull : ((1ull << hist) - 1ull);
+        const int sh = kg * KT * 16 + 2 * c;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          // window rows visible to this row (slots below the sequence's Wb only)
+          const uint64_t anc = (h ? anc1 : anc0) & ((1u << Wb) - 1u);
+          // window slot w sits at page key L + w - key0p
+          const int off = L - key0p;
+          uint64_t wmask = 0;
+          if (off >= 0 && off < kPage) wmask = anc << off;
+          else if (off < 0 && off > -32) wmask = anc >> (-off);
+          const uint64_t m = valid[h] ? (hmask | wmask) >> sh : 0ull;
+          uint32_t bits = 0;
+#pragma unroll
+          for (int t = 0; t < 2 * KT; ++t)
+            bits |= (uint32_t)((m >> (t * 8)) & 3ull) << (2 * t);
+          vb[h] = bits;
+        }
+      }
 #pragma unroll
       for (int t = 0; t < 2 * KT; ++t) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int h = e >> 1;
-          const int tkey = key0 + t * 8 + 2 * c + (e & 1);
-          const uint32_t anc = h ? anc1 : anc0;
-          bool vis = tkey < L || (tkey < n_keys && ((anc >> (tkey - L)) & 1u));
-          vis = vis && valid[h];
-          const float v = vis ? sc[t][e] * scale_log2 : -INFINITY;
+          const float v = ((vb[h] >> (t * 2 + (e & 1))) & 1u) ? sc[t][e] * scale_log2 : -INFINITY;
           sc[t][e] = v;
           mx[h] = fmaxf(mx[h], v);
         }
@@ -367,44 +395,46 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32)
   if (warp == n_cons) pdl_wait();  // every thread below may write the output
   cluster.sync();
   if (!s_fail) {
-    // CTA `rank` merges rows rank, rank + 8, ...  First the per-row weights
-    // w_s = 2^(m_s - max m) / sum_s 2^(m_s - max m) l_s (one pass over the 8 CTAs'
-    // (m, l), kept in registers of the row's lane), then each output element is
-    // sum_s w_s o_s[d] with the 8 remote loads independent of each other.
+    // CTA `rank` merges rows rank, rank + CS, ...: each thread owns 4 consecutive
+    // output elements of one row and issues all of its remote loads -- the CS
+    // CTAs' (m, l) of the row and their 4 partial outputs -- before using any,
+    // so the merge costs one round trip over distributed shared memory.
+    // out = sum_s 2^(m_s - max m) o_s / sum_s 2^(m_s - max m) l_s
+    constexpr int V4 = HD / 4;
     const int n_my_rows = rows > rank ? (rows - rank + CS - 1) / CS : 0;
-    if (threadIdx.x < n_my_rows) {
-      const int r = rank + threadIdx.x * CS;
+    const uint32_t o_base = smem_u32(part_o), m_base = smem_u32(part_m), l_base = smem_u32(part_l);
+    for (int it = threadIdx.x; it < n_my_rows * V4; it += blockDim.x) {
+      const int lr = it / V4, d4 = it % V4;
+      const int r = rank + lr * CS;
       float ms[CS], ls[CS];
+      float4 os[CS];
+#pragma unroll
+      for (int s = 0; s < CS; ++s) {
+        ms[s] = ld_dsmem_f32(mapa_u32(m_base + r * 4, s));
+        ls[s] = ld_dsmem_f32(mapa_u32(l_base + r * 4, s));
+        os[s] = ld_dsmem_f4(mapa_u32(o_base + (r * HD + d4 * 4) * 4, s));
+      }
       float mmax = -INFINITY;
 #pragma unroll
-      for (int s = 0; s < CS; ++s) {
-        ms[s] = cluster.map_shared_rank(part_m, s)[r];
-        ls[s] = cluster.map_shared_rank(part_l, s)[r];
-        mmax = fmaxf(mmax, ms[s]);
-      }
-      float den = 0.f;
+      for (int s = 0; s < CS; ++s) mmax = fmaxf(mmax, ms[s]);
+      float den = 0.f, n0 = 0.f, n1 = 0.f, n2 = 0.f, n3 = 0.f;
 #pragma unroll
       for (int s = 0; s < CS; ++s) {
-        ms[s] = (mmax == -INFINITY || ms[s] == -INFINITY) ? 0.f : fast_exp2(ms[s] - mmax);
-        den += ms[s] * ls[s];
+        const float w = (mmax == -INFINITY || ms[s] == -INFINITY) ? 0.f : fast_exp2(ms[s] - mmax);
+        den += w * ls[s];
+        n0 += w * os[s].x;
+        n1 += w * os[s].y;
+        n2 += w * os[s].z;
+        n3 += w * os[s].w;
       }
       const float inv = den > 0.f ? 1.f / den : 0.f;
-#pragma unroll
-      for (int s = 0; s < CS; ++s) wts[threadIdx.x * CS + s] = ms[s] * inv;
-    }
-    __syncthreads();
-    for (int e = threadIdx.x; e < n_my_rows * HD; e += blockDim.x) {
-      const int lr = e / HD;
-      const int r = rank + lr * CS;
-      const int d = e % HD;
-      float o[CS];
-#pragma unroll
-      for (int s = 0; s < CS; ++s) o[s] = cluster.map_shared_rank(part_o, s)[r * HD + d];
-      float num = 0.f;
-#pragma unroll
-      for (int s = 0; s < CS; ++s) num += wts[lr * CS + s] * o[s];
       const int j = r / grp, hq = kvh * grp + r % grp;
-      p.out[((long long)(row0 + j) * p.Hq + hq) * HD + d] = to_act(num);
+      __half2 lo = __halves2half2(to_act(n0 * inv), to_act(n1 * inv));
+      __half2 hi = __halves2half2(to_act(n2 * inv), to_act(n3 * inv));
+      uint2 pk;
+      pk.x = *reinterpret_cast<uint32_t*>(&lo);
+      pk.y = *reinterpret_cast<uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(p.out + ((long long)(row0 + j) * p.Hq + hq) * HD + d4 * 4) = pk;
     }
   }
   // keep this CTA's shared memory alive until every CTA has read it

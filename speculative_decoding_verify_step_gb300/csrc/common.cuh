@@ -93,6 +93,28 @@ SPEC_DEVICE_INLINE void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// Hint: bring [src, src + bytes) into L2 (bulk copy engine; nothing waits on it).
+// src 16-byte aligned, bytes a multiple of 16.
+SPEC_DEVICE_INLINE void l2_prefetch_bulk(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
+               : "memory");
+}
+
+// This CTA's share (by linear block index) of [base, base + bytes) brought into
+// L2 in pieces of at most 64 KB; bytes a multiple of 16.
+SPEC_DEVICE_INLINE void l2_prefetch_share(const void* base, unsigned long long bytes) {
+  if (!base || bytes == 0) return;
+  const unsigned long long nblk = (unsigned long long)gridDim.x * gridDim.y * gridDim.z;
+  const unsigned long long cta = blockIdx.x + (unsigned long long)gridDim.x * (blockIdx.y + (unsigned long long)gridDim.y * blockIdx.z);
+  const unsigned long long units = bytes >> 4;  // 16-byte units
+  const unsigned long long u1 = units * (cta + 1) / nblk;
+  const char* b = static_cast<const char*>(base);
+  for (unsigned long long u = units * cta / nblk; u < u1; u += 4096) {
+    const unsigned long long n = u1 - u < 4096 ? u1 - u : 4096;
+    l2_prefetch_bulk(b + (u << 4), (uint32_t)(n << 4));
+  }
+}
+
 // 2-D tiled load (coordinates: c0 innermost, in elements) completing on `bar`.
 SPEC_DEVICE_INLINE void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
   asm volatile(
@@ -133,6 +155,12 @@ SPEC_DEVICE_INLINE uint32_t mapa_u32(uint32_t a, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
   return r;
+}
+
+SPEC_DEVICE_INLINE float ld_dsmem_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
 }
 
 SPEC_DEVICE_INLINE float4 ld_dsmem_f4(uint32_t addr) {

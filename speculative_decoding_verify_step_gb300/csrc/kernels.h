@@ -84,6 +84,11 @@ struct AttnParams {
   int sm_count;                // picks the cluster size (1 to 16 CTAs per sequence and kv head)
   int kv_len_hint;             // upper bound of L + W over the batch (launch shape only)
   uint32_t anc[16];            // ancestor masks of the window rows (bit i: row i visible)
+  // Weights of the projections that follow, brought into L2 once the QKV
+  // projection is done (HBM is otherwise idle while a short-context attention
+  // runs); split evenly over the CTAs.  Null / 0: none.
+  const void* l2_next[2];
+  unsigned long long l2_next_bytes[2];  // multiples of 16
   __half* out;                 // [M, Hq*hd]
   int* status;
 };
