@@ -429,12 +429,8 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32)
       }
       const float inv = den > 0.f ? 1.f / den : 0.f;
       const int j = r / grp, hq = kvh * grp + r % grp;
-      __half2 lo = __halves2half2(to_act(n0 * inv), to_act(n1 * inv));
-      __half2 hi = __halves2half2(to_act(n2 * inv), to_act(n3 * inv));
-      uint2 pk;
-      pk.x = *reinterpret_cast<uint32_t*>(&lo);
-      pk.y = *reinterpret_cast<uint32_t*>(&hi);
-      *reinterpret_cast<uint2*>(p.out + ((long long)(row0 + j) * p.Hq + hq) * HD + d4 * 4) = pk;
+      *reinterpret_cast<uint2*>(p.out + ((long long)(row0 + j) * p.Hq + hq) * HD + d4 * 4) =
+          pack_act4(n0 * inv, n1 * inv, n2 * inv, n3 * inv);
     }
   }
   // keep this CTA's shared memory alive until every CTA has read it

@@ -27,6 +27,15 @@ constexpr unsigned long long kWaitBudgetCycles = 4000000000ull;  // ~2 s at 2 GH
 // of 8; accumulation is fp32 throughout.
 using act_t = __half;
 SPEC_DEVICE_INLINE act_t to_act(float x) { return __float2half_rn(fminf(fmaxf(x, -65504.f), 65504.f)); }
+// Four values as four consecutive act_t (8 bytes, for one aligned store).
+SPEC_DEVICE_INLINE uint2 pack_act4(float a, float b, float c, float d) {
+  __half2 lo = __halves2half2(to_act(a), to_act(b));
+  __half2 hi = __halves2half2(to_act(c), to_act(d));
+  uint2 r;
+  r.x = *reinterpret_cast<uint32_t*>(&lo);
+  r.y = *reinterpret_cast<uint32_t*>(&hi);
+  return r;
+}
 
 // ---------------------------------------------------------------- status word
 // First error wins; kernels that hit an error skip the offending accesses.

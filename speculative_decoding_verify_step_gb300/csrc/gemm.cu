@@ -149,9 +149,14 @@ SPEC_DEVICE_INLINE void epi_prefetch(const EpiParams& p, EpiPre<EPI, NT, ROWS>& 
 // memory, in split order (deterministic), and runs the epilogue on those rows --
 // the reduction is spread over the S CTAs and never leaves the chip.  The caller
 // holds back the CTA's exit with the matching cluster_wait().
-template <int EPI, int NT, int ROWS>
+//
+// PREP: the weight-row scales, the row scales and (QKV) the rows' positions and
+// KV slots were already placed in s_rs / s_scale / s_ps while the mainloop ran;
+// U: items of the split-K reduction in flight per thread.
+template <int EPI, int NT, int ROWS, bool PREP = false, int U = 1>
 SPEC_DEVICE_INLINE void finish_tile(const EpiParams& p, const EpiPre<EPI, NT, ROWS>& pre, float* tile,
-                                    float* s_scale, int m0, int n0, int tid, int warp, int lane) {
+                                    float* s_scale, int m0, int n0, int tid, int warp, int lane,
+                                    float* s_rs_prep = nullptr, const int2* s_ps = nullptr) {
   using E = EpiPre<EPI, NT, ROWS>;
   constexpr int kGroupWarps = NT / 32;
   int r_lo, r_hi;
@@ -160,32 +165,44 @@ SPEC_DEVICE_INLINE void finish_tile(const EpiParams& p, const EpiPre<EPI, NT, RO
     cluster_arrive();  // this CTA's partial tile is written
     cluster_wait();    // ... and every other split's
     const int S = p.splits;
-    for (int e = tid; e < max(0, r_hi - r_lo) * (kBN / 4); e += NT) {
-      const int ml = r_lo + e / (kBN / 4), cl = (e % (kBN / 4)) * 4;
-      const uint32_t off = smem_u32(tile + ml * kTilePad + cl);
-      float4 a[kMaxSplits];
+    const int n_items = max(0, r_hi - r_lo) * (kBN / 4);
+    // U items per thread at a time: all of their remote loads are issued first
+    for (int e0 = tid; e0 < n_items; e0 += U * NT) {
+      float4 a[U][kMaxSplits];
 #pragma unroll
-      for (int j = 0; j < kMaxSplits; ++j)
-        if (j < S) a[j] = ld_dsmem_f4(mapa_u32(off, j));
-      float4 v = a[0];
+      for (int u = 0; u < U; ++u) {
+        const int e = min(e0 + u * NT, n_items - 1);
+        const uint32_t off = smem_u32(tile + (r_lo + e / (kBN / 4)) * kTilePad + (e % (kBN / 4)) * 4);
 #pragma unroll
-      for (int j = 1; j < kMaxSplits; ++j)
-        if (j < S) {
-          v.x += a[j].x;
-          v.y += a[j].y;
-          v.z += a[j].z;
-          v.w += a[j].w;
-        }
-      *reinterpret_cast<float4*>(&tile[ml * kTilePad + cl]) = v;
+        for (int j = 0; j < kMaxSplits; ++j)
+          if (j < S) a[u][j] = ld_dsmem_f4(mapa_u32(off, j));
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int e = e0 + u * NT;
+        if (e >= n_items) break;
+        float4 v = a[u][0];
+#pragma unroll
+        for (int j = 1; j < kMaxSplits; ++j)
+          if (j < S) {
+            v.x += a[u][j].x;
+            v.y += a[u][j].y;
+            v.z += a[u][j].z;
+            v.w += a[u][j].w;
+          }
+        *reinterpret_cast<float4*>(&tile[(r_lo + e / (kBN / 4)) * kTilePad + (e % (kBN / 4)) * 4]) = v;
+      }
     }
     cluster_arrive();  // done reading the other CTAs' tiles
   }
   // weight-row scale 2^-e of the fp16 encoding, per output column of the tile
-  __shared__ float s_rs[kBN];
+  __shared__ float s_rs_own[kBN];
+  float* s_rs = PREP ? s_rs_prep : s_rs_own;
   // per-row scale of a normalised input: s_m = rsqrt(sum_t ssq[t][m] / d + eps).
   // One warp per row, tiles lane, lane + 32, ... per lane (then a fixed shuffle
   // tree: the same order on every run).
-  if constexpr (E::kOn) {
+  if constexpr (PREP) {
+  } else if constexpr (E::kOn) {
     if (tid < kBN) s_rs[tid] = pre.rs;
 #pragma unroll
     for (int k = 0; k < E::kRowsW; ++k) {
@@ -255,7 +272,67 @@ SPEC_DEVICE_INLINE void finish_tile(const EpiParams& p, const EpiPre<EPI, NT, RO
         dst[i + half] = to_act(b);
       }
     };
-    if constexpr (E::kOn) {
+    if constexpr (PREP) {
+      // four consecutive pairs (i .. i+3 of one head) per item, eight items per
+      // thread at a time: their angles are loaded together, then written as
+      // 8-byte groups
+      const int n_quads = n_pairs / 4;
+      constexpr int kB = 8;
+      for (int e0 = tid; e0 < n_quads; e0 += kB * NT) {
+        float4 cs[kB], sn[kB];
+#pragma unroll
+        for (int j = 0; j < kB; ++j) {
+          const int e = min(e0 + j * NT, n_quads - 1);
+          const int ml = r_lo + e / (kBN / 8), pr = (e % (kBN / 8)) * 4;
+          const int i = (n0 + (pr / half) * p.hd + pr % half) % p.hd;
+          const long long a = (long long)s_ps[ml].x * half + i;
+          cs[j] = __ldg(reinterpret_cast<const float4*>(p.rope_cos + a));
+          sn[j] = __ldg(reinterpret_cast<const float4*>(p.rope_sin + a));
+        }
+#pragma unroll
+        for (int j = 0; j < kB; ++j) {
+          const int e = e0 + j * NT;
+          if (e >= n_quads) break;
+          const int ml = r_lo + e / (kBN / 8), pr = (e % (kBN / 8)) * 4;
+          const int m = m0 + ml;
+          const int cl = (pr / half) * p.hd + pr % half;
+          const int n = n0 + cl;
+          const int head = n / p.hd, i = n % p.hd;
+          const float sc = s_scale[ml];
+          const float4 ta = *reinterpret_cast<const float4*>(&tile[ml * kTilePad + cl]);
+          const float4 tb = *reinterpret_cast<const float4*>(&tile[ml * kTilePad + cl + half]);
+          const float4 ra = *reinterpret_cast<const float4*>(&s_rs[cl]);
+          const float4 rb = *reinterpret_cast<const float4*>(&s_rs[cl + half]);
+          float av[4] = {ta.x * (sc * ra.x), ta.y * (sc * ra.y), ta.z * (sc * ra.z), ta.w * (sc * ra.w)};
+          float bv[4] = {tb.x * (sc * rb.x), tb.y * (sc * rb.y), tb.z * (sc * rb.z), tb.w * (sc * rb.w)};
+          if (head < p.Hq + p.Hkv) {
+            const float c4[4] = {cs[j].x, cs[j].y, cs[j].z, cs[j].w};
+            const float s4[4] = {sn[j].x, sn[j].y, sn[j].z, sn[j].w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float x = av[k] * c4[k] - bv[k] * s4[k];
+              const float y = av[k] * s4[k] + bv[k] * c4[k];
+              av[k] = x;
+              bv[k] = y;
+            }
+          }
+          act_t* dst = nullptr;
+          if (head < p.Hq) {
+            dst = p.q_out + ((long long)m * p.Hq + head) * p.hd;
+          } else if (s_ps[ml].y >= 0) {  // slot < 0: the round failed to get a page for this row
+            const int slot = s_ps[ml].y;
+            const bool is_k = head < p.Hq + p.Hkv;
+            const int kvh = is_k ? head - p.Hq : head - p.Hq - p.Hkv;
+            dst = (is_k ? p.kpool : p.vpool) +
+                  (((long long)(slot / kPage) * p.Hkv + kvh) * kPage + slot % kPage) * p.hd;
+          }
+          if (dst) {
+            *reinterpret_cast<uint2*>(dst + i) = pack_act4(av[0], av[1], av[2], av[3]);
+            *reinterpret_cast<uint2*>(dst + i + half) = pack_act4(bv[0], bv[1], bv[2], bv[3]);
+          }
+        }
+      }
+    } else if constexpr (E::kOn) {
 #pragma unroll
       for (int k = 0; k < E::kPairs; ++k) {
         const int e = tid + k * NT;
@@ -328,8 +405,9 @@ SPEC_DEVICE_INLINE void finish_tile(const EpiParams& p, const EpiPre<EPI, NT, RO
       float gn[kBN / 32];
 #pragma unroll
       for (int j = 0; j < kBN / 32; ++j) gn[j] = p.g_next[n0 + lane + 32 * j];
-      // four rows per warp at a time: their residuals are loaded before any is written
-      constexpr int kB = 4;
+      // four (eight when the scales were prepared: registers are free) rows per
+      // warp at a time: their residuals are loaded before any is written
+      constexpr int kB = PREP ? 8 : 4;
       for (int r0 = r_lo + warp; r0 < r_hi; r0 += kB * kGroupWarps) {
         float rin[kB][kBN / 32];
 #pragma unroll
@@ -556,8 +634,41 @@ struct TcCfg {
   static constexpr int kTileBytes = NT * kTilePad * 4;
   static_assert(kTileBytes <= kPipeBytes, "epilogue tile reuses the pipeline buffers");
   static constexpr int kTmemCols = NT;  // fp32 accumulator: one column per token row
-  static constexpr int kSmemBytes = kPipeBytes + (2 * kStages + 1) * 8 + 16 + NT * 4 + 1024;
+  // barriers, TMEM address, row scales [NT], weight-row scales [kBN], (position, slot) [NT]
+  static constexpr int kSmemBytes = kPipeBytes + (2 * kStages + 1) * 8 + 16 + 16 + NT * 4 + kBN * 4 + NT * 8 + 1024;
 };
+
+// Epilogue inputs that do not depend on the accumulator, placed in shared memory
+// by the four TMEM warps (t = 0..127) while the MMAs run: the weight-row scales
+// of the tile's columns, the row scale of each row this split finishes (sum of
+// the previous kernel's per-tile r^2, in the same order as the epilogue would)
+// and, for QKV, each row's position and KV slot.
+template <int EPI, int NT>
+SPEC_DEVICE_INLINE void tc_prep(const EpiParams& p, int m0, int n0, float* s_scale, float* s_rs, int2* s_ps, int t,
+                                int w, int lane) {
+  int r_lo, r_hi;
+  tile_rows<NT>(p, m0, r_lo, r_hi);
+  s_rs[t] = __ldg(p.rscale + n0 + t);
+  for (int r0 = r_lo + w; r0 < r_hi; r0 += 8 * 4) {  // eight rows per warp at a time
+    float ss[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int r = r0 + j * 4;
+      float a = 0.f;
+      if (r < r_hi && p.ssq_in)
+        for (int tt = lane; tt < p.ssq_tiles; tt += 32) a += __ldcg(p.ssq_in + (long long)tt * p.ssq_stride + m0 + r);
+      ss[j] = a;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int r = r0 + j * 4;
+      const float sum = warp_sum(ss[j]);
+      if (r < r_hi && lane == 0) s_scale[r] = p.ssq_in ? rsqrtf(sum * p.inv_d + p.eps) : 1.f;
+    }
+  }
+  if constexpr (EPI == kEpiQKV)
+    for (int r = r_lo + t; r < r_hi; r += 128) s_ps[r] = make_int2(__ldcg(p.row_pos + m0 + r), __ldcg(p.row_slot + m0 + r));
+}
 
 template <int NT, int EPI>
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -570,7 +681,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* empty = full + C::kStages;
   uint64_t* accum = empty + C::kStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
-  float* s_scale = reinterpret_cast<float*>(tmem_slot + 4);
+  // 16-byte aligned: the epilogue reads s_rs as float4
+  float* s_scale = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(tmem_slot + 4) + 15) & ~uintptr_t(15));
+  float* s_rs = s_scale + NT;
+  int2* s_ps = reinterpret_cast<int2*>(s_rs + kBN);
   __shared__ int s_fail;
 
   const int warp = threadIdx.x >> 5;
@@ -655,6 +769,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     pdl_launch_dependents();
     const int q = warp & 3;            // TMEM lane quarter this warp may access
     const int nl = q * 32 + lane;      // weight row of this thread within the tile
+    tc_prep<EPI, NT>(p, m0, n0, s_scale, s_rs, s_ps, threadIdx.x - 64, warp - 2, lane);
     const bool done = mbar_wait(accum, 0, p.status);
     tc_fence_after();
     if (!done) s_fail = 1;
@@ -688,8 +803,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   if (warp < 2) pdl_wait();  // outputs are written below by every warp
   EpiPre<EPI, kTcThreads, NT> pre;  // loads its epilogue inputs row by row
-  finish_tile<EPI, kTcThreads, NT>(p, pre, reinterpret_cast<float*>(smem), s_scale, m0, n0, threadIdx.x, warp,
-                                   lane);
+  finish_tile<EPI, kTcThreads, NT, true, 2>(p, pre, reinterpret_cast<float*>(smem), s_scale, m0, n0, threadIdx.x,
+                                            warp, lane, s_rs, s_ps);
   if (p.splits > 1) cluster_wait();  // the other splits are done reading this CTA's tile
 }
 

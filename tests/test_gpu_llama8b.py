@@ -198,7 +198,7 @@ def test_top1_and_nucleus_rounds_at_full_vocab(two_layer):
         assert int(c4[b, n]) in set(nuc.tolist())
 
 
-@pytest.mark.parametrize("B,W", [(1, 16), (4, 8)])
+@pytest.mark.parametrize("B,W", [(1, 16), (4, 8), (8, 12)])
 def test_repeated_scores_are_bit_identical(two_layer, B, W):
     """Every reduction of the path runs in a fixed order, so scoring the same window
     again gives the same bits.  Catches pipeline races (a stage refilled while it is
