@@ -179,6 +179,11 @@ spec_status validate_cfg(const spec_config& c) {
 
 // Bytes HBM moves during a latency-bound attention launch (~10 us at ~6.5 TB/s).
 constexpr double kAttnL2Budget = 64e6;
+// Bytes of the next projection's weights prefetched into L2 at the end of each
+// projection's weight stream (HBM idles while its grid drains, ~2-3 us).  Only
+// while the projections are weight streams (<= 32 token rows; measured: neutral
+// to slightly negative on the tensor-core path).
+constexpr double kProjL2Budget = 16e6;
 
 long long max_len_bound(const spec_model* m) {
   long long b = 0;
@@ -274,6 +279,7 @@ spec_status forward(spec_model* m, int B, int W, const int32_t* seq_ids, const i
   const double pf = std::max(0.0, kAttnL2Budget - kv_bytes);
   const unsigned long long pf_o = (unsigned long long)std::min(pf, wb_o) & ~15ull;
   const unsigned long long pf_gu = (unsigned long long)std::max(0.0, std::min(pf - (double)pf_o, wb_gu)) & ~15ull;
+  const double proj_pf = BM <= 32 ? kProjL2Budget : 0.0;
   for (int l = 0; l < c.n_layers; ++l) {
     auto& Ly = m->layers[l];
     ap.l2_next[0] = Ly.wo;
@@ -313,6 +319,8 @@ spec_status forward(spec_model* m, int B, int W, const int32_t* seq_ids, const i
       e.xn = m->xn;
       e.ssq_out = m->ssq_b;
       e.d = d;
+      e.l2_next = reinterpret_cast<const char*>(Ly.wgu) + pf_gu;
+      e.l2_next_bytes = (unsigned long long)std::min(proj_pf, wb_gu - (double)pf_gu) & ~15ull;
       CUDA_TRY(profiled(m, 1, wb_o, st, [&] { return launch_gemm_epi(kEpiResid, &Ly.tm_o, &m->tm_attn[bi], BM, e, st); }));
     }
     {
@@ -324,6 +332,8 @@ spec_status forward(spec_model* m, int B, int W, const int32_t* seq_ids, const i
       e.ssq_in = m->ssq_b;
       e.act = m->act;
       e.ffn = F;
+      e.l2_next = Ly.wdown;
+      e.l2_next_bytes = (unsigned long long)std::min(proj_pf, wb_dn) & ~15ull;
       CUDA_TRY(profiled(m, 2, wb_gu, st, [&] { return launch_gemm_epi(kEpiSwiGLU, &Ly.tm_gu, &m->tm_xn[bi], BM, e, st); }));
     }
     {
@@ -338,6 +348,13 @@ spec_status forward(spec_model* m, int B, int W, const int32_t* seq_ids, const i
       e.xn = m->xn;
       e.ssq_out = m->ssq_a;
       e.d = d;
+      if (l + 1 < c.n_layers) {
+        e.l2_next = m->layers[l + 1].wqkv;
+        e.l2_next_bytes = (unsigned long long)std::min(proj_pf, wb_qkv) & ~15ull;
+      } else if (want_logits) {
+        e.l2_next = m->lm_head;
+        e.l2_next_bytes = (unsigned long long)std::min(proj_pf, 2.0 * c.vocab * d) & ~15ull;
+      }
       CUDA_TRY(profiled(m, 3, wb_dn, st, [&] { return launch_gemm_epi(kEpiResid, &Ly.tm_down, &m->tm_act[bi], BM, e, st); }));
     }
   }

@@ -98,8 +98,9 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32)
   // griddepcontrol.wait, which it does before letting this kernel launch; only
   // q and the window's K/V come from the predecessor itself.  The successor (the
   // O projection) only prefetches weights before its own wait, so it may launch
-  // right away.
-  pdl_launch_dependents();
+  // right away -- or, for short attentions (p.late_trigger), once this CTA's
+  // queries have arrived: its weight stream would otherwise queue ahead of them.
+  if (!p.late_trigger) pdl_launch_dependents();
   const int sid = p.seq_ids[b];
   const bool sid_ok = sid >= 0 && sid < p.max_batch;  // a bad id was flagged by the prepare kernel
   const int L = p.seq_start[b];
@@ -172,10 +173,16 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32)
   } else {
     // ---------------------------------------------------------------- consumers
     pdl_wait();  // q is written by the QKV projection
-    if (warp == 0 && lane == 0) {
-      l2_prefetch_share(p.l2_next[0], p.l2_next_bytes[0]);
-      l2_prefetch_share(p.l2_next[1], p.l2_next_bytes[1]);
-    }
+    // the successor may launch, and the next weights go to L2: at once, or (late
+    // trigger) after this warp's first use of its queries
+    auto release_successor = [&] {
+      if (warp == 0 && lane == 0) {
+        if (p.late_trigger) pdl_launch_dependents();
+        l2_prefetch_share(p.l2_next[0], p.l2_next_bytes[0]);
+        l2_prefetch_share(p.l2_next[1], p.l2_next_bytes[1]);
+      }
+    };
+    if (!p.late_trigger) release_successor();
     const int g = lane >> 2, c = lane & 3;
     const int rt = warp / KG, kg = warp % KG;  // row tile, key group (keys kg*16*KT .. of each page)
     // query rows of this thread: r0 = rt*16 + g, r1 = r0 + 8; row r -> window row j = r / grp
@@ -238,6 +245,7 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32)
           mma_f16_16816(sc[2 * tp + 1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
         }
       }
+      if (p.late_trigger && i == 0) release_successor();
       // mask + online softmax (exp2 domain)
       const int key0 = (pg0 + i) * kPage + kg * KT * 16;
       float mx[2] = {-INFINITY, -INFINITY};
@@ -332,6 +340,7 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32)
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     }
+    if (p.late_trigger && npg == 0) release_successor();
     // drained: every issued page was consumed, so the stage buffers are free
     // once all consumer warps are here (named barrier over the consumers)
     asm volatile("bar.sync 1, %0;" ::"r"(n_cons * 32) : "memory");
@@ -462,10 +471,12 @@ cudaError_t launch_attention_hd(const CUtensorMap* tmK, const CUtensorMap* tmV, 
   const int row_tiles = (rows + 15) / 16;
   if (row_tiles > kMaxRowTiles) return cudaErrorInvalidValue;
   const int pages_per_cta = ((p.kv_len_hint + kPage - 1) / kPage + CS - 1) / CS;
+  AttnParams q = p;
+  q.late_trigger = pages_per_cta <= 2;  // measured: earlier successor launch wins from 3 pages per CTA
   switch (key_groups(row_tiles, pages_per_cta)) {
-    case 4: return launch_attention_kg<HD, CS, 4>(tmK, tmV, p, row_tiles, st);
-    case 2: return launch_attention_kg<HD, CS, 2>(tmK, tmV, p, row_tiles, st);
-    default: return launch_attention_kg<HD, CS, 1>(tmK, tmV, p, row_tiles, st);
+    case 4: return launch_attention_kg<HD, CS, 4>(tmK, tmV, q, row_tiles, st);
+    case 2: return launch_attention_kg<HD, CS, 2>(tmK, tmV, q, row_tiles, st);
+    default: return launch_attention_kg<HD, CS, 1>(tmK, tmV, q, row_tiles, st);
   }
 }
 

@@ -478,9 +478,9 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * kBN;
+  const int n0 = blockIdx.z * kBN;
   const int split = blockIdx.y;
-  const int m0 = blockIdx.z * BM;
+  const int m0 = blockIdx.x * BM;
   const int kb0 = split * p.kb_per_split;
   const int nkb = min(p.kb_per_split, p.kb_total - kb0);
 
@@ -519,6 +519,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         tma_load_2d_hint(stage_w(s), &tmW, (kb0 + kb) * kBK, n0, &full[s], pol);
         tma_load_2d(stage_x(s), &tmX, (kb0 + kb) * kBK, m0, &full[s]);
       }
+      l2_prefetch_share(p.l2_next, p.l2_next_bytes);
     }
     __syncwarp();
     if (p.splits > 1) {  // the two cluster barriers of the split-K reduction
@@ -689,9 +690,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * kBN;
+  const int n0 = blockIdx.z * kBN;
   const int split = blockIdx.y;
-  const int m0 = blockIdx.z * NT;
+  const int m0 = blockIdx.x * NT;
   const int kb0 = split * p.kb_per_split;
   const int nkb = min(p.kb_per_split, p.kb_total - kb0);
 
@@ -738,6 +739,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tma_load_2d_hint(stage_w(s), &tmW, (kb0 + kb) * kBK, n0, &full[s], pol);
         tma_load_2d(stage_x(s), &tmX, (kb0 + kb) * kBK, m0, &full[s]);
       }
+      l2_prefetch_share(p.l2_next, p.l2_next_bytes);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -839,7 +841,9 @@ template <int BM, int EPI>
 cudaError_t launch_proj(const CUtensorMap* tmW, const CUtensorMap* tmX, const EpiParams& p, cudaStream_t st) {
   using K = Kern<BM, EPI>;
   if (cudaError_t e = configure<BM, EPI>()) return e;
-  dim3 grid(p.N / kBN, p.splits, (p.M + BM - 1) / BM);
+  // token tiles fastest: the tiles of one weight slab are dispatched side by side,
+  // so a slab streamed from HBM for one token tile is still in L2 for the next
+  dim3 grid((p.M + BM - 1) / BM, p.splits, p.N / kBN);
   if (p.splits == 1) return launch_k(K::fn(), grid, dim3(K::kThreadsPerCta), K::kSmem, st, *tmW, *tmX, p);
   return launch_k_cluster(K::fn(), grid, dim3(K::kThreadsPerCta), K::kSmem, st, dim3(1, p.splits, 1), *tmW, *tmX,
                           p);

@@ -54,6 +54,11 @@ struct EpiParams {
   float* tstat_sum;                    // null: greedy (no sum)
   int32_t* tstat_arg;
   int tstat_stride;
+  // Weights of the next projection, brought into L2 by each CTA's producer once
+  // its own weight stream is issued (HBM idles while the grid drains and the next
+  // kernel starts); split evenly over the CTAs.  Null / 0: none.
+  const void* l2_next;
+  unsigned long long l2_next_bytes;  // multiple of 16
   int* status;
 };
 cudaError_t launch_gemm_epi(int epi, const CUtensorMap* tmW, const CUtensorMap* tmX, int BM, EpiParams p,
@@ -89,6 +94,7 @@ struct AttnParams {
   // runs); split evenly over the CTAs.  Null / 0: none.
   const void* l2_next[2];
   unsigned long long l2_next_bytes[2];  // multiples of 16
+  int late_trigger;            // set by the launcher: release the successor after the queries arrive
   __half* out;                 // [M, Hq*hd]
   int* status;
 };
