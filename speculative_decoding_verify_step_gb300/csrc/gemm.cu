@@ -693,6 +693,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int n0 = blockIdx.z * kBN;
   const int split = blockIdx.y;
   const int m0 = blockIdx.x * NT;
+  const int n_act = min(NT, (p.M - m0 + 15) & ~15);  // token rows the MMAs cover
   const int kb0 = split * p.kb_per_split;
   const int nkb = min(p.kb_per_split, p.kb_total - kb0);
 
@@ -745,7 +746,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   } else if (warp == 1) {
     // ----------------------------------------------------- MMA issue (1 thread)
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_f16_f32(kBN, NT);
+      // MMA width: the tile's token rows rounded up to 16 (a ragged last tile
+      // multiplies only its own rows)
+      const uint32_t idesc = idesc_f16_f32(kBN, n_act);
       int kb = 0;
       for (; kb < nkb; ++kb) {
         const int s = kb % C::kStages;
@@ -778,7 +781,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     float* tile = reinterpret_cast<float*>(smem);  // MMAs and loads are done with the stages
     if (done) {
 #pragma unroll 1
-      for (int c0 = 0; c0 < NT; c0 += 16) {
+      for (int c0 = 0; c0 < n_act; c0 += 16) {
         float v[16];
         tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + c0, v);
 #pragma unroll
