@@ -141,6 +141,70 @@ SPEC_DEVICE_INLINE void epi_prefetch(const EpiParams& p, EpiPre<EPI, NT, ROWS>& 
   }
 }
 
+// Split-K reduction of this split's rows: item e = (row r_lo + e / 32, columns
+// 4 (e % 32) ..+3); each item sums the S CTAs' partials in split order (the same
+// order on every run).  U items per thread are in flight at a time, their S
+// remote loads each issued before any is used.
+template <int S, int U, int NT>
+SPEC_DEVICE_INLINE void reduce_rows(float* tile, int r_lo, int n_items, int tid) {
+  for (int e0 = tid; e0 < n_items; e0 += U * NT) {
+    float4 a[U][S];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int e = min(e0 + u * NT, n_items - 1);
+      const uint32_t off = smem_u32(tile + (r_lo + e / (kBN / 4)) * kTilePad + (e % (kBN / 4)) * 4);
+#pragma unroll
+      for (int j = 0; j < S; ++j) a[u][j] = ld_dsmem_f4(mapa_u32(off, j));
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int e = e0 + u * NT;
+      if (e >= n_items) break;
+      float4 v = a[u][0];
+#pragma unroll
+      for (int j = 1; j < S; ++j) {
+        v.x += a[u][j].x;
+        v.y += a[u][j].y;
+        v.z += a[u][j].z;
+        v.w += a[u][j].w;
+      }
+      *reinterpret_cast<float4*>(&tile[(r_lo + e / (kBN / 4)) * kTilePad + (e % (kBN / 4)) * 4]) = v;
+    }
+  }
+}
+
+template <int NT, int LOADS, int S = 2>
+SPEC_DEVICE_INLINE void reduce_splits(int splits, float* tile, int r_lo, int n_items, int tid) {
+  if constexpr (LOADS == 1) {
+    // one item at a time: a single loop for every split count (measured: the
+    // specialised copies cost more in instruction fetch than they save here)
+    for (int e = tid; e < n_items; e += NT) {
+      const int ml = r_lo + e / (kBN / 4), cl = (e % (kBN / 4)) * 4;
+      const uint32_t off = smem_u32(tile + ml * kTilePad + cl);
+      float4 a[kMaxSplits];
+#pragma unroll
+      for (int j = 0; j < kMaxSplits; ++j)
+        if (j < splits) a[j] = ld_dsmem_f4(mapa_u32(off, j));
+      float4 v = a[0];
+#pragma unroll
+      for (int j = 1; j < kMaxSplits; ++j)
+        if (j < splits) {
+          v.x += a[j].x;
+          v.y += a[j].y;
+          v.z += a[j].z;
+          v.w += a[j].w;
+        }
+      *reinterpret_cast<float4*>(&tile[ml * kTilePad + cl]) = v;
+    }
+  } else if constexpr (S <= kMaxSplits) {
+    if (splits == S) {
+      reduce_rows<S, (LOADS / S > 1 ? LOADS / S : 1), NT>(tile, r_lo, n_items, tid);
+    } else {
+      reduce_splits<NT, LOADS, S + 1>(splits, tile, r_lo, n_items, tid);
+    }
+  }
+}
+
 // The end of a tile, common to both projection kernels.  Called by the NT
 // epilogue threads (tid 0..NT-1, warp = tid / 32) once this CTA's accumulator is
 // in `tile` (its own shared memory).  With split-K the splits of a tile form one
@@ -152,8 +216,8 @@ SPEC_DEVICE_INLINE void epi_prefetch(const EpiParams& p, EpiPre<EPI, NT, ROWS>& 
 //
 // PREP: the weight-row scales, the row scales and (QKV) the rows' positions and
 // KV slots were already placed in s_rs / s_scale / s_ps while the mainloop ran;
-// U: items of the split-K reduction in flight per thread.
-template <int EPI, int NT, int ROWS, bool PREP = false, int U = 1>
+// LOADS: remote float4 loads of the split-K reduction in flight per thread.
+template <int EPI, int NT, int ROWS, bool PREP = false, int LOADS = 1>
 SPEC_DEVICE_INLINE void finish_tile(const EpiParams& p, const EpiPre<EPI, NT, ROWS>& pre, float* tile,
                                     float* s_scale, int m0, int n0, int tid, int warp, int lane,
                                     float* s_rs_prep = nullptr, const int2* s_ps = nullptr) {
@@ -164,35 +228,7 @@ SPEC_DEVICE_INLINE void finish_tile(const EpiParams& p, const EpiPre<EPI, NT, RO
   if (p.splits > 1) {
     cluster_arrive();  // this CTA's partial tile is written
     cluster_wait();    // ... and every other split's
-    const int S = p.splits;
-    const int n_items = max(0, r_hi - r_lo) * (kBN / 4);
-    // U items per thread at a time: all of their remote loads are issued first
-    for (int e0 = tid; e0 < n_items; e0 += U * NT) {
-      float4 a[U][kMaxSplits];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int e = min(e0 + u * NT, n_items - 1);
-        const uint32_t off = smem_u32(tile + (r_lo + e / (kBN / 4)) * kTilePad + (e % (kBN / 4)) * 4);
-#pragma unroll
-        for (int j = 0; j < kMaxSplits; ++j)
-          if (j < S) a[u][j] = ld_dsmem_f4(mapa_u32(off, j));
-      }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int e = e0 + u * NT;
-        if (e >= n_items) break;
-        float4 v = a[u][0];
-#pragma unroll
-        for (int j = 1; j < kMaxSplits; ++j)
-          if (j < S) {
-            v.x += a[u][j].x;
-            v.y += a[u][j].y;
-            v.z += a[u][j].z;
-            v.w += a[u][j].w;
-          }
-        *reinterpret_cast<float4*>(&tile[(r_lo + e / (kBN / 4)) * kTilePad + (e % (kBN / 4)) * 4]) = v;
-      }
-    }
+    reduce_splits<NT, LOADS>(p.splits, tile, r_lo, max(0, r_hi - r_lo) * (kBN / 4), tid);
     cluster_arrive();  // done reading the other CTAs' tiles
   }
   // weight-row scale 2^-e of the fp16 encoding, per output column of the tile
@@ -672,7 +708,7 @@ SPEC_DEVICE_INLINE void tc_prep(const EpiParams& p, int m0, int n0, float* s_sca
 }
 
 template <int NT, int EPI>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(kTcThreads, NT <= 128 ? 2 : 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    const __grid_constant__ EpiParams p) {
   using C = TcCfg<NT>;
@@ -808,7 +844,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   if (warp < 2) pdl_wait();  // outputs are written below by every warp
   EpiPre<EPI, kTcThreads, NT> pre;  // loads its epilogue inputs row by row
-  finish_tile<EPI, kTcThreads, NT, true, 2>(p, pre, reinterpret_cast<float*>(smem), s_scale, m0, n0, threadIdx.x,
+  finish_tile<EPI, kTcThreads, NT, true, 8>(p, pre, reinterpret_cast<float*>(smem), s_scale, m0, n0, threadIdx.x,
                                             warp, lane, s_rs, s_ps);
   if (p.splits > 1) cluster_wait();  // the other splits are done reading this CTA's tile
 }
