@@ -92,6 +92,9 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32)
   const int n_cons = blockDim.x / 32 - 1;  // consumer warps: (row tile, key group) pairs
   const int grp = p.Hq / p.Hkv;
   constexpr int KT = 4 / KG;                // 16-key tiles of a page per consumer warp
+  // key-group partials go straight into the cluster merge while it stays small
+  // (CS * KG partials per row); above that each CTA first combines its own
+  constexpr bool kFoldKg = KG > 1 && CS * KG <= 16;
 
   // Sequence state and the cached pages were written by kernels that completed
   // before the QKV projection (this kernel's predecessor) passed its own
@@ -247,7 +250,6 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32)
       }
       if (p.late_trigger && i == 0) release_successor();
       // mask + online softmax (exp2 domain)
-      const int key0 = (pg0 + i) * kPage + kg * KT * 16;
       float mx[2] = {-INFINITY, -INFINITY};
       // visibility of the page's 64 keys for this thread's two rows (bit k: key
       // key0p + k), then of this thread's keys of the slice (bit t*2 + (e&1))
@@ -362,7 +364,7 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32)
         l_dst[r] = valid[h] ? lrow[h] : 0.f;
       }
     }
-    if constexpr (KG > 1) {
+    if constexpr (KG > 1 && !kFoldKg) {
     asm volatile("bar.sync 1, %0;" ::"r"(n_cons * 32) : "memory");
     // combine the KG partials of every row: weights 2^(m_kg - max m), then O, m, l
     const int n_rows_launch = (n_cons / KG) * 16;
@@ -405,30 +407,49 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32)
   cluster.sync();
   if (!s_fail) {
     // CTA `rank` merges rows rank, rank + CS, ...: each thread owns 4 consecutive
-    // output elements of one row and issues all of its remote loads -- the CS
-    // CTAs' (m, l) of the row and their 4 partial outputs -- before using any,
-    // so the merge costs one round trip over distributed shared memory.
-    // out = sum_s 2^(m_s - max m) o_s / sum_s 2^(m_s - max m) l_s
+    // output elements of one row and issues all of its remote loads -- the (m, l)
+    // of the row's partials and their 4 partial outputs -- before using any, so
+    // the merge costs one round trip over distributed shared memory.  The
+    // partials are the CS CTAs' (and, when folded, each CTA's KG key groups').
+    // out = sum_p 2^(m_p - max m) o_p / sum_p 2^(m_p - max m) l_p
     constexpr int V4 = HD / 4;
+    constexpr int KGM = kFoldKg ? KG : 1;  // key-group partials per CTA in the merge
+    constexpr int NP = CS * KGM;
     const int n_my_rows = rows > rank ? (rows - rank + CS - 1) / CS : 0;
     const uint32_t o_base = smem_u32(part_o), m_base = smem_u32(part_m), l_base = smem_u32(part_l);
+    const uint32_t ko_base = smem_u32(kg_o), km_base = smem_u32(kg_m), kl_base = smem_u32(kg_l);
     for (int it = threadIdx.x; it < n_my_rows * V4; it += blockDim.x) {
       const int lr = it / V4, d4 = it % V4;
       const int r = rank + lr * CS;
-      float ms[CS], ls[CS];
-      float4 os[CS];
+      const int rtr = r / 16, rr = r % 16;
+      float ms[NP], ls[NP];
+      float4 os[NP];
 #pragma unroll
       for (int s = 0; s < CS; ++s) {
-        ms[s] = ld_dsmem_f32(mapa_u32(m_base + r * 4, s));
-        ls[s] = ld_dsmem_f32(mapa_u32(l_base + r * 4, s));
-        os[s] = ld_dsmem_f4(mapa_u32(o_base + (r * HD + d4 * 4) * 4, s));
+#pragma unroll
+        for (int k = 0; k < KGM; ++k) {
+          uint32_t ma, la, oa;
+          if (k == 0) {
+            ma = m_base + r * 4;
+            la = l_base + r * 4;
+            oa = o_base + (r * HD + d4 * 4) * 4;
+          } else {
+            const int sl = (rtr * (KG - 1) + k - 1) * 16 + rr;
+            ma = km_base + sl * 4;
+            la = kl_base + sl * 4;
+            oa = ko_base + (sl * HD + d4 * 4) * 4;
+          }
+          ms[s * KGM + k] = ld_dsmem_f32(mapa_u32(ma, s));
+          ls[s * KGM + k] = ld_dsmem_f32(mapa_u32(la, s));
+          os[s * KGM + k] = ld_dsmem_f4(mapa_u32(oa, s));
+        }
       }
       float mmax = -INFINITY;
 #pragma unroll
-      for (int s = 0; s < CS; ++s) mmax = fmaxf(mmax, ms[s]);
+      for (int s = 0; s < NP; ++s) mmax = fmaxf(mmax, ms[s]);
       float den = 0.f, n0 = 0.f, n1 = 0.f, n2 = 0.f, n3 = 0.f;
 #pragma unroll
-      for (int s = 0; s < CS; ++s) {
+      for (int s = 0; s < NP; ++s) {
         const float w = (mmax == -INFINITY || ms[s] == -INFINITY) ? 0.f : fast_exp2(ms[s] - mmax);
         den += w * ls[s];
         n0 += w * os[s].x;
