@@ -917,13 +917,21 @@ int max_active_clusters(int s) {
   return cache[s];
 }
 
+static_assert(TcCfg<64>::kSmemBytes <= GemmCfg<8>::kSmemBytes && TcCfg<128>::kSmemBytes <= GemmCfg<8>::kSmemBytes &&
+                  kTcThreads <= kThreads,
+              "the mma.sync kernel's footprint bounds the 64/128-row tcgen05 kernel's");
+
 int max_active_clusters_bm(int BM, int s) {
   switch (BM) {
     case 8: return max_active_clusters<8>(s);
     case 16: return max_active_clusters<16>(s);
     case 32: return max_active_clusters<32>(s);
-    case 64: return max_active_clusters<64>(s);
-    case 128: return max_active_clusters<128>(s);
+    // The occupancy calculator reports one CTA per SM for the tcgen05 kernel
+    // whatever its footprint (measured), while two of its 64- and 128-row CTAs
+    // (~100 KB of shared memory, <= 128 TMEM columns each) do run side by side;
+    // the mma.sync kernel's two-per-SM footprint stands in for the cluster count.
+    case 64:
+    case 128: return max_active_clusters<8>(s);
     default: return max_active_clusters<256>(s);
   }
 }
