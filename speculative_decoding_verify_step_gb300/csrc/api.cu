@@ -75,8 +75,8 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-constexpr int kNumBM = 6;
-constexpr int kBMs[kNumBM] = {8, 16, 32, 64, 128, 256};
+constexpr int kNumBM = 5;
+constexpr int kBMs[kNumBM] = {8, 16, 32, 64, 128};
 int bm_index(int bm) {
   for (int i = 0; i < kNumBM; ++i)
     if (kBMs[i] == bm) return i;

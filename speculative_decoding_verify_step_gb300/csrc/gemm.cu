@@ -653,8 +653,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 // ----------------------------------------------------------------------------
 // tcgen05 path from 64 token rows: the same weight stream, but the
 // contraction runs on the 5th-generation tensor cores.  One CTA = 128 weight
-// rows x NT token rows (NT in 32..256, so up to 256 rows stream each weight
-// tile exactly once).  Warp 0 drives TMA, one thread of warp 1 issues
+// rows x NT token rows (NT = 64 or 128; more rows take several token tiles,
+// dispatched side by side so that one weight slab serves them from L2).  Warp 0 drives TMA, one thread of warp 1 issues
 // tcgen05.mma (A = 128 weight rows, B = NT token rows, both K-major with the
 // 128-byte swizzle, fp32 accumulator in TMEM) and commits each stage back to the
 // producer; warps 2..5 read the accumulator out of TMEM (each warp its 32-lane
@@ -663,7 +663,8 @@ constexpr int kTcThreads = 192;
 
 template <int NT>
 struct TcCfg {
-  static constexpr int kStages = NT == 256 ? 4 : (NT == 128 ? 3 : (NT == 64 ? 4 : 5));
+  static_assert(NT == 64 || NT == 128, "token tiles of 64 or 128 rows (two CTAs per SM)");
+  static constexpr int kStages = NT == 128 ? 3 : 4;
   static constexpr int kWBytes = kBN * kBK * 2;
   static constexpr int kXBytes = NT * kBK * 2;
   static constexpr int kStageBytes = kWBytes + kXBytes;
@@ -708,7 +709,7 @@ SPEC_DEVICE_INLINE void tc_prep(const EpiParams& p, int m0, int n0, float* s_sca
 }
 
 template <int NT, int EPI>
-__global__ void __launch_bounds__(kTcThreads, NT <= 128 ? 2 : 1)
+__global__ void __launch_bounds__(kTcThreads, 2)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    const __grid_constant__ EpiParams p) {
   using C = TcCfg<NT>;
@@ -930,9 +931,7 @@ int max_active_clusters_bm(int BM, int s) {
     // whatever its footprint (measured), while two of its 64- and 128-row CTAs
     // (~100 KB of shared memory, <= 128 TMEM columns each) do run side by side;
     // the mma.sync kernel's two-per-SM footprint stands in for the cluster count.
-    case 64:
-    case 128: return max_active_clusters<8>(s);
-    default: return max_active_clusters<256>(s);
+    default: return max_active_clusters<8>(s);  // 64 and 128 rows
   }
 }
 
@@ -945,7 +944,6 @@ cudaError_t launch_epi(const CUtensorMap* tmW, const CUtensorMap* tmX, int BM, c
     case 32: return launch_proj<32, EPI>(tmW, tmX, p, st);
     case 64: return launch_proj<64, EPI>(tmW, tmX, p, st);
     case 128: return launch_proj<128, EPI>(tmW, tmX, p, st);
-    case 256: return launch_proj<256, EPI>(tmW, tmX, p, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -953,12 +951,13 @@ cudaError_t launch_epi(const CUtensorMap* tmW, const CUtensorMap* tmX, int BM, c
 }  // namespace
 
 int choose_bm(int M) {
+  // beyond 128 rows: several 128-row tiles (measured: two 128-row CTAs per SM
+  // beat one 256-row CTA, 7-11% on whole rounds of 192-320 rows)
   if (M <= 8) return 8;
   if (M <= 16) return 16;
   if (M <= 32) return 32;
   if (M <= 64) return 64;
-  if (M <= 128) return 128;
-  return 256;
+  return 128;
 }
 
 int choose_splits(int N, int K, int M, int BM, int sm_count, int max_splits) {

@@ -1,7 +1,7 @@
 """GPU parity at the Llama-3.1-8B widths (d 4096, 32/8 heads of 128, ffn 14336,
 vocab 128256).  A 2-layer model is compared with the oracle element by element at
-row counts that take both projection paths (<= 64 rows: mma.sync; 96 and 208
-rows: tcgen05); the full 32-layer model, in the launch configuration the bench
+row counts that take both projection paths (<= 32 rows: mma.sync; from 64 rows:
+tcgen05 in 64- or 128-row token tiles, 208 rows as two); the full 32-layer model, in the launch configuration the bench
 times (B = 1, 1024 cached tokens), is checked through properties that hold at any
 size and through the oracle's page allocator."""
 import numpy as np
