@@ -523,7 +523,9 @@ def profiled_traffic(cls):
         return None, "no traffic line"
     if m.group(1) != blob:
         return None, "stale: projection source changed since the capture"
-    return int(t.group(1)), "profiles/gemm_swapab_llama8b_m5.md"
+    n = re.search(r"traffic-note\s+" + re.escape(cls) + r":\s*(.+)", text)
+    src_s = "profiles/gemm_swapab_llama8b_m5.md" + (" (" + n.group(1).strip() + ")" if n else "")
+    return int(t.group(1)), src_s
 
 
 def weight_bytes(dims):
