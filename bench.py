@@ -497,7 +497,7 @@ class Bench:
                     "speedup_vs_decode": round(theta[best] / theta[1], 3),
                     "width_aligned_to_token_tile": planner.align_to_tile(best, B, 16)}
         return {"step_ms": table, "planner": plan, "widths": list(widths),
-                "note": "rows per weight stream come in tiles of 8/16/32/64/128 (more rows: several 128-row tiles); T is nearly flat inside one"}
+                "note": "rows per weight stream come in tiles of 8/16/64/128 (more rows: several 128-row tiles); T is nearly flat inside one"}
 
     def _barrier(self):
         torch = self.torch

@@ -75,8 +75,8 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-constexpr int kNumBM = 5;
-constexpr int kBMs[kNumBM] = {8, 16, 32, 64, 128};
+constexpr int kNumBM = 4;
+constexpr int kBMs[kNumBM] = {8, 16, 64, 128};
 int bm_index(int bm) {
   for (int i = 0; i < kNumBM; ++i)
     if (kBMs[i] == bm) return i;
@@ -181,7 +181,7 @@ spec_status validate_cfg(const spec_config& c) {
 constexpr double kAttnL2Budget = 64e6;
 // Bytes of the next projection's weights prefetched into L2 at the end of each
 // projection's weight stream (HBM idles while its grid drains, ~2-3 us).  Only
-// while the projections are weight streams (<= 32 token rows; measured: neutral
+// while the projections are weight streams (mma.sync tiles, <= 16 token rows; measured: neutral
 // to slightly negative on the tensor-core path).
 constexpr double kProjL2Budget = 16e6;
 
@@ -279,7 +279,7 @@ spec_status forward(spec_model* m, int B, int W, const int32_t* seq_ids, const i
   const double pf = std::max(0.0, kAttnL2Budget - kv_bytes);
   const unsigned long long pf_o = (unsigned long long)std::min(pf, wb_o) & ~15ull;
   const unsigned long long pf_gu = (unsigned long long)std::max(0.0, std::min(pf - (double)pf_o, wb_gu)) & ~15ull;
-  const double proj_pf = BM <= 32 ? kProjL2Budget : 0.0;
+  const double proj_pf = BM <= 16 ? kProjL2Budget : 0.0;
   for (int l = 0; l < c.n_layers; ++l) {
     auto& Ly = m->layers[l];
     ap.l2_next[0] = Ly.wo;

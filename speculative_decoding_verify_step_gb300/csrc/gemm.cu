@@ -926,7 +926,6 @@ int max_active_clusters_bm(int BM, int s) {
   switch (BM) {
     case 8: return max_active_clusters<8>(s);
     case 16: return max_active_clusters<16>(s);
-    case 32: return max_active_clusters<32>(s);
     // The occupancy calculator reports one CTA per SM for the tcgen05 kernel
     // whatever its footprint (measured), while two of its 64- and 128-row CTAs
     // (~100 KB of shared memory, <= 128 TMEM columns each) do run side by side;
@@ -938,10 +937,9 @@ int max_active_clusters_bm(int BM, int s) {
 template <int EPI>
 cudaError_t launch_epi(const CUtensorMap* tmW, const CUtensorMap* tmX, int BM, const EpiParams& p,
                        cudaStream_t st) {
-  switch (BM) {  // up to 32 token rows: mma.sync (HBM-bound); from 64: tcgen05
+  switch (BM) {  // up to 16 token rows: mma.sync (HBM-bound); from 17: tcgen05
     case 8: return launch_proj<8, EPI>(tmW, tmX, p, st);
     case 16: return launch_proj<16, EPI>(tmW, tmX, p, st);
-    case 32: return launch_proj<32, EPI>(tmW, tmX, p, st);
     case 64: return launch_proj<64, EPI>(tmW, tmX, p, st);
     case 128: return launch_proj<128, EPI>(tmW, tmX, p, st);
     default: return cudaErrorInvalidValue;
@@ -951,11 +949,12 @@ cudaError_t launch_epi(const CUtensorMap* tmW, const CUtensorMap* tmX, int BM, c
 }  // namespace
 
 int choose_bm(int M) {
-  // beyond 128 rows: several 128-row tiles (measured: two 128-row CTAs per SM
-  // beat one 256-row CTA, 7-11% on whole rounds of 192-320 rows)
+  // measured on whole rounds: mma.sync up to 16 rows; tcgen05 64-row tiles (MMA
+  // width = rows rounded up to 16) from 17 rows, 6-7% faster than mma.sync at
+  // 20-30 rows and 8% slower at 16; beyond 128 rows several 128-row tiles (two
+  // 128-row CTAs per SM beat one 256-row CTA by 7-11% at 192-320 rows)
   if (M <= 8) return 8;
   if (M <= 16) return 16;
-  if (M <= 32) return 32;
   if (M <= 64) return 64;
   return 128;
 }

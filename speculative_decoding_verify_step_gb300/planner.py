@@ -7,9 +7,9 @@ predicts the step time of that budget from a cost table measured on the device,
 and picks the budget with the largest progress per unit of step time; rows up to
 the execution tier that is paid for anyway verify extra candidates at almost no
 cost ("align verify tokens to the graph tier").  Here the tier is the token tile
-of the projection kernels: one weight stream serves up to 8, 16, 32, 64 or 128
-token rows (more rows take several 128-row tiles side by side), so the step time is
-nearly flat inside a tile.
+of the projection kernels: one weight stream serves up to 8, 16, 64 or 128 token
+rows (more rows take several 128-row tiles side by side), so the step time is nearly
+flat inside a tile.
 
 The trained confidence head that supplies per-candidate survival probabilities
 is not part of this library; callers pass survival probabilities (for example
@@ -19,7 +19,7 @@ from __future__ import annotations
 
 from typing import Dict, Mapping, Sequence, Tuple
 
-TOKEN_TILES = (8, 16, 32, 64, 128)
+TOKEN_TILES = (8, 16, 64, 128)
 
 
 def survival_iid(alpha: float, n: int) -> list:

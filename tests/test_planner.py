@@ -42,9 +42,9 @@ def test_flat_and_steep_cost_curves():
 
 def test_token_tiles_and_alignment():
     assert [P.token_tile(r) for r in (1, 8, 9, 16, 17, 64, 65, 200, 256, 300)] == \
-        [8, 8, 16, 16, 32, 64, 128, 256, 256, 384]
+        [8, 8, 16, 16, 64, 64, 128, 256, 256, 384]
     assert P.align_to_tile(5, 1, 16) == 8       # 5 rows -> tile of 8: verify 8
-    assert P.align_to_tile(5, 4, 16) == 8       # 20 rows -> tile of 32: 32 rows = width 8
+    assert P.align_to_tile(5, 4, 16) == 16      # 20 rows -> tile of 64: 64 rows = width 16
     assert P.align_to_tile(3, 16, 16) == 4      # 48 rows -> tile of 64
     assert P.align_to_tile(9, 1, 12) == 12      # capped by the widest window
     for B, w in itertools.product((1, 2, 3, 7, 16), range(1, 17)):
