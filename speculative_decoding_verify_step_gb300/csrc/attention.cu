@@ -504,12 +504,17 @@ cudaError_t launch_attention_hd(const CUtensorMap* tmK, const CUtensorMap* tmV, 
 }  // namespace
 
 cudaError_t launch_attention(const CUtensorMap* tmK, const CUtensorMap* tmV, const AttnParams& p, cudaStream_t st) {
-  // 16-CTA clusters while they still fit in one wave (two CTAs per SM), else 8
-  // the widest cluster (16, 8, 4, 2 or 1 CTAs per sequence and kv head) whose grid
-  // still fits in one wave at two CTAs per SM: few sequences spread their pages over
-  // many SMs, many sequences keep more pages per CTA (and fewer merges)
+  // The widest cluster (16, 8, 4, 2 or 1 CTAs per sequence and kv head) whose grid
+  // fits one CTA per SM, while that still gives at least 4; else the widest that
+  // fits two per SM.  Few sequences spread their pages over many SMs, many keep
+  // more pages per CTA (and fewer merges).  Measured: a 16-CTA cluster doubled up
+  // on SMs (B = 2) is 7% slower per round than an 8-CTA cluster alone on them.
   int cs = 16;
-  while (cs > 1 && p.B * p.Hkv * cs > 2 * p.sm_count) cs >>= 1;
+  while (cs > 1 && p.B * p.Hkv * cs > p.sm_count) cs >>= 1;
+  if (cs < 4) {
+    cs = 16;
+    while (cs > 1 && p.B * p.Hkv * cs > 2 * p.sm_count) cs >>= 1;
+  }
   if (p.hd == 128) {
     switch (cs) {
       case 16: return launch_attention_hd<128, 16>(tmK, tmV, p, st);
