@@ -37,6 +37,22 @@ namespace {
 
 constexpr int kAccThreads = 1024;
 
+// Accept tests of drafts 1..gamma, evaluated side by side by one warp (lane i
+// tests draft i: 1 accept, 0 reject, -1 invalid token) instead of one after the
+// other: the accepted prefix ends at the first failing test, and an invalid token
+// there is flagged (the tests past it cannot change the outcome).  All lanes of
+// the calling warp return the prefix length; gamma < 32.
+template <typename Test>
+SPEC_DEVICE_INLINE int accepted_prefix(int gamma, int lane, int* status, Test&& test) {
+  const bool mine = lane >= 1 && lane <= gamma;
+  const int r = mine ? test(lane) : 1;
+  const unsigned fail = __ballot_sync(0xffffffffu, mine && r != 1);
+  if (fail == 0u) return gamma;
+  const int f = __ffs(fail) - 1;  // first failing draft
+  if (lane == f && r < 0) set_status(status, SPEC_ERR_INVALID_ARG);
+  return f - 1;
+}
+
 struct ArgMax {
   float v;
   int i;
@@ -175,26 +191,22 @@ __global__ void __launch_bounds__(kAccThreads) accept_chain_kernel(const __grid_
   }
   auto am = [&](int row) -> int { return p.row_argmax ? p.row_argmax[row0 + row] : s_am[row]; };
 
-  if (threadIdx.x == 0) {
-    int n = 0;
-    for (int i = 1; i <= p.gamma; ++i) {
+  if (threadIdx.x < 32) {
+    const int n = accepted_prefix(p.gamma, threadIdx.x, p.status, [&](int i) -> int {
       const int x = xdraft(i);
-      bool acc;
-      if (x < 0 || x >= V) {
-        set_status(p.status, SPEC_ERR_INVALID_ARG);
-        acc = false;
-      } else if constexpr (SAMPLED) {
+      if (x < 0 || x >= V) return -1;
+      if constexpr (SAMPLED) {
         const float qx = p.q[((long long)b * p.gamma + (i - 1)) * V + x];
-        acc = __fmul_rn(p.u[row0 + i - 1], qx) < prob(i - 1, x);
+        return __fmul_rn(p.u[row0 + i - 1], qx) < prob(i - 1, x) ? 1 : 0;
       } else {
-        acc = x == am(i - 1);
+        return x == am(i - 1) ? 1 : 0;
       }
-      if (!acc) break;
-      ++n;
+    });
+    if (threadIdx.x == 0) {
+      s_n = n;
+      s_zero = 0;
+      if constexpr (!SAMPLED) s_tok = am(n);
     }
-    s_n = n;
-    s_zero = 0;
-    if constexpr (!SAMPLED) s_tok = am(n);
   }
   __syncthreads();
   const int n = s_n;
@@ -342,24 +354,18 @@ __global__ void __launch_bounds__(kAccThreads) accept_round_kernel(const __grid_
   };
   auto xdraft = [&](int i) -> int { return p.tok[row0 + i]; };  // x_i = window row i
 
-  if (threadIdx.x == 0) {
-    int n = 0;
-    for (int i = 1; i <= gamma; ++i) {
+  if (warp == 0) {
+    const int n = accepted_prefix(gamma, threadIdx.x, p.status, [&](int i) -> int {
       const int x = xdraft(i);
-      bool acc;
-      if (x < 0 || x >= V) {
-        set_status(p.status, SPEC_ERR_INVALID_ARG);
-        acc = false;
-      } else if constexpr (SAMPLED) {
+      if (x < 0 || x >= V) return -1;
+      if constexpr (SAMPLED) {
         const float qx = p.q[((long long)b * p.gamma + (i - 1)) * V + x];
-        acc = __fmul_rn(p.u[urow + i - 1], qx) < prob(i - 1, x);
+        return __fmul_rn(p.u[urow + i - 1], qx) < prob(i - 1, x) ? 1 : 0;
       } else {
-        acc = x == s_am[i - 1];
+        return x == s_am[i - 1] ? 1 : 0;
       }
-      if (!acc) break;
-      ++n;
-    }
-    s_n = n;
+    });
+    if (threadIdx.x == 0) s_n = n;
   }
   __syncthreads();
   const int n = s_n;
