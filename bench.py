@@ -63,6 +63,8 @@ def parse_args():
                     help="skip the batch sweep, the 32K-context and the tree workloads")
     ap.add_argument("--cpu-layers", type=int, default=2, help="layers in the oracle's timed sample")
     ap.add_argument("--quick", action="store_true", help="a short run for profilers: timed replay only")
+    ap.add_argument("--top-p", type=float, default=None,
+                    help="profiler mode only: nucleus sampling on every row (adds the selection kernel)")
     ap.add_argument("--ncu", action="store_true",
                     help="profiler mode: cache filled directly (no prefill), fixed drafts, W + K verify rounds")
     return ap.parse_args()
@@ -706,8 +708,9 @@ def run_ncu_mode(args):
     u = synth.uniforms((B, W), seed=6, device=dev)
     outs = None
     torch.cuda.synchronize()
+    tp = None if args.top_p is None else [args.top_p] * B
     for _ in range(args.warmup + args.steps):
-        outs = m.verify_step(ids, tok, q=q, u=u, temperature=args.temperature, outs=outs)
+        outs = m.verify_step(ids, tok, q=q, u=u, temperature=args.temperature, outs=outs, top_p=tp)
     torch.cuda.synchronize()
     m.sync_status()
     print(json.dumps({"ncu_mode": True, "layers": args.layers, "launches_per_round": m.last_launch_count(),
