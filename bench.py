@@ -507,19 +507,30 @@ class Bench:
             torch.distributed.barrier()
 
 
+def code_sha1(path):
+    """sha1 of a C++/CUDA source without its // comments and blank lines: the
+    identity of the code an ncu capture was taken from (comment edits keep it)."""
+    import hashlib
+    import re
+    lines = []
+    for line in open(path).read().splitlines():
+        line = re.sub(r"//.*$", "", line).rstrip()
+        if line.strip():
+            lines.append(line)
+    return hashlib.sha1("\n".join(lines).encode()).hexdigest()
+
+
 def profiled_traffic(cls):
     """DRAM bytes per launch of projection class `cls` from the committed ncu summary,
     if that summary was taken from the current projection source (else None)."""
-    import hashlib
     import re
     src = os.path.join(ROOT, "speculative_decoding_verify_step_gb300", "csrc", "gemm.cu")
     summ = os.path.join(ROOT, "profiles", "gemm_swapab_llama8b_m5.md")
     if not (os.path.exists(src) and os.path.exists(summ)):
         return None, "no profile"
-    data = open(src, "rb").read()
-    blob = hashlib.sha1(b"blob %d\0" % len(data) + data).hexdigest()
+    blob = code_sha1(src)
     text = open(summ).read()
-    m = re.search(r"source-blob:\s*([0-9a-f]{40})", text)
+    m = re.search(r"source-code-sha1:\s*([0-9a-f]{40})", text)
     t = re.search(r"traffic-bytes-per-launch\s+" + re.escape(cls) + r":\s*([0-9]+)", text)
     if not m or not t:
         return None, "no traffic line"

@@ -8,11 +8,13 @@
 // Decode" section 9.1: ~129 tokens ride in the shadow of the weight read at
 // batch 1).  So the kernel is built around the weight stream:
 //   * one producer warp drives a multi-stage TMA pipeline of 128 x 64 fp16
-//     weight tiles (the bf16 weights re-encoded exactly as fp16 x 2^e per row) (128-byte swizzle, L2 evict-first) plus the matching BM x 64
-//     activation tile, completing on mbarriers;
+//     weight tiles (the bf16 weights re-encoded exactly as fp16 x 2^e per row;
+//     128-byte swizzle, L2 evict-first) plus the matching BM x 64 activation
+//     tile, completing on mbarriers, then prefetches the start of the next
+//     projection's weights into L2;
 //   * eight consumer warps each own 16 weight rows and run mma.sync m16n8k16
 //     with the weights as the A operand ("swap-AB": weight rows on the MMA M
-//     side, token rows on N, so 1..64 tokens need no padding to 64);
+//     side, token rows on N, so 1..16 tokens need no padding to 64);
 //   * split-K over gridDim.y fills the 152 SMs when N/128 tiles are few.  The
 //     splits of a tile run as one thread-block cluster: each keeps its fp32
 //     partial tile in its own shared memory, and after a cluster barrier split r
@@ -21,6 +23,8 @@
 //     epilogue to those rows;
 //   * the weight prefetch is issued before griddepcontrol.wait, so under
 //     programmatic dependent launch it overlaps the previous kernel's tail.
+// This mma.sync kernel serves up to 16 token rows; from 17 rows the tcgen05
+// kernel below takes over (tiles of 64 or 128 token rows).
 //
 // RMSNorm is folded in: the producer of a normalised input stores
 // X' = fp16(r * g) and per-128-column partial sums of r^2; the consumer scales
@@ -651,14 +655,15 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 
 // ----------------------------------------------------------------------------
-// tcgen05 path from 64 token rows: the same weight stream, but the
-// contraction runs on the 5th-generation tensor cores.  One CTA = 128 weight
-// rows x NT token rows (NT = 64 or 128; more rows take several token tiles,
-// dispatched side by side so that one weight slab serves them from L2).  Warp 0 drives TMA, one thread of warp 1 issues
-// tcgen05.mma (A = 128 weight rows, B = NT token rows, both K-major with the
-// 128-byte swizzle, fp32 accumulator in TMEM) and commits each stage back to the
-// producer; warps 2..5 read the accumulator out of TMEM (each warp its 32-lane
-// quarter) and run the same tile finish as the mma.sync path.
+// tcgen05 path from 17 token rows: the same weight stream, but the contraction
+// runs on the 5th-generation tensor cores.  One CTA = 128 weight rows x NT token
+// rows (NT = 64 or 128; more rows take several token tiles, dispatched side by
+// side so that one weight slab serves them from L2).  Warp 0 drives TMA, one
+// thread of warp 1 issues tcgen05.mma (A = 128 weight rows, B = the tile's token
+// rows, both K-major with the 128-byte swizzle, fp32 accumulator in TMEM) and
+// commits each stage back to the producer; warps 2..5 stage the epilogue inputs,
+// read the accumulator out of TMEM (each warp its 32-lane quarter) and, with the
+// other two warps, run the same tile finish as the mma.sync path.
 constexpr int kTcThreads = 192;
 
 template <int NT>
@@ -853,7 +858,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
 // Kernel, block size and dynamic shared memory of the projection for a token tile.
 template <int BM, int EPI>
 struct Kern {
-  static constexpr bool kTc = BM >= 64;  // tcgen05 from 64 token rows (measured: mma.sync is faster at 32)
+  static constexpr bool kTc = BM >= 64;  // tcgen05 tiles of 64 / 128 token rows (chosen from 17 rows)
   static auto fn() {
     if constexpr (kTc) {
       return gemm_tc_kernel<BM, EPI>;
@@ -961,9 +966,8 @@ int choose_bm(int M) {
 
 int choose_splits(int N, int K, int M, int BM, int sm_count, int max_splits) {
   // The most splits (cluster size) for which every tile's cluster is resident in
-  // one wave (shared memory allows two CTAs per SM up to 128 token rows, one
-  // above; the GPC layout limits how many clusters fit), with every split
-  // non-empty and at least 4 k-blocks long.
+  // one wave (two CTAs per SM for every token tile; the GPC layout limits how
+  // many clusters fit), with every split non-empty and at least 4 k-blocks long.
   const int tiles = (N / kBN) * ((M + BM - 1) / BM);
   const int kb = K / kBK;
   const int slots = (BM <= 128 ? 2 : 1) * sm_count;
