@@ -282,27 +282,37 @@ class Bench:
         return e0.elapsed_time(e1) / reps
 
     def replay_e2e(self, rounds, warmup, temp):
-        """Same rounds, inputs from pinned host memory and outputs read back every step."""
+        """Same rounds, inputs from pinned host memory and outputs read back every step.
+        Each step's inputs (tokens, q, u) travel as one host-to-device copy and its
+        outputs (accepted, committed, bonus) as one device-to-host copy: one pinned
+        buffer each way, the tensors are views into it."""
         torch = self.torch
         B, W = self.B, rounds[0][0].shape[1]
-        host = [(t.cpu().pin_memory(), q.cpu().pin_memory(), u.cpu().pin_memory()) for t, q, u in rounds]
-        d_tok = torch.empty_like(rounds[0][0])
-        d_q = torch.empty_like(rounds[0][1])
-        d_u = torch.empty_like(rounds[0][2])
-        outs = (torch.empty(B, dtype=torch.int32, device=self.dev), torch.empty(B, W, dtype=torch.int32,
-                                                                                device=self.dev),
-                torch.empty(B, dtype=torch.int32, device=self.dev))
-        h_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+        parts = [(x.dtype, tuple(x.shape), x.numel() * x.element_size()) for x in rounds[0]]
+        offs = [0]
+        for _, _, nb in parts:  # each part 256-byte aligned, like its own allocation
+            offs.append(offs[-1] + (nb + 255) // 256 * 256)
+
+        def views(buf):
+            return [buf[offs[i]:offs[i] + nb].view(dt).view(sh) for i, (dt, sh, nb) in enumerate(parts)]
+
+        host = []
+        for r in rounds:
+            hb = torch.empty(offs[-1], dtype=torch.uint8).pin_memory()
+            for v, x in zip(views(hb), r):
+                v.copy_(x.cpu())
+            host.append(hb)
+        d_in = torch.empty(offs[-1], dtype=torch.uint8, device=self.dev)
+        d_tok, d_q, d_u = views(d_in)
+        d_out = torch.empty(B + B * W + B, dtype=torch.int32, device=self.dev)
+        outs = (d_out[:B], d_out[B:B + B * W].view(B, W), d_out[B + B * W:])
+        h_out = torch.empty(d_out.shape, dtype=torch.int32).pin_memory()
         acc_log = []
 
         def step(r):
-            t, q, u = host[r]
-            d_tok.copy_(t, non_blocking=True)
-            d_q.copy_(q, non_blocking=True)
-            d_u.copy_(u, non_blocking=True)
+            d_in.copy_(host[r], non_blocking=True)
             self.model.verify_step(self.ids, d_tok, q=d_q, u=d_u, temperature=temp, outs=outs)
-            for h, o in zip(h_out, outs):
-                h.copy_(o, non_blocking=True)
+            h_out.copy_(d_out, non_blocking=True)
 
         self.reset()
         for r in range(warmup):
@@ -314,13 +324,12 @@ class Bench:
         for r in range(warmup, len(rounds)):
             step(r)
             torch.cuda.current_stream().synchronize()   # the host reads this step's result
-            acc_log.append(h_out[0].clone())
+            acc_log.append(h_out[:B].clone())
         e1.record()
         torch.cuda.synchronize()
         self._barrier()
-        h2d = sum(x.numel() * x.element_size() for x in host[0])
-        d2h = sum(o.numel() * o.element_size() for o in outs)
-        return e0.elapsed_time(e1), torch.stack(acc_log), h2d, d2h
+        return (e0.elapsed_time(e1), torch.stack(acc_log), sum(nb for _, _, nb in parts),
+                d_out.numel() * d_out.element_size())
 
     def profile(self, rounds, warmup, temp, n):
         self.reset()
