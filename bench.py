@@ -75,6 +75,19 @@ def dist_env():
         int(os.environ.get("WORLD_SIZE", "1"))
 
 
+def whole_job(ms, tokens, device="cpu"):
+    """Whole-job (time, tokens) over the ranks: the slowest rank's time, the sum of
+    the tokens.  One rank (no process group): the values themselves."""
+    import torch
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return float(ms), float(tokens)
+    mx = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    sm = torch.tensor([float(tokens)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(mx, op=torch.distributed.ReduceOp.MAX)
+    torch.distributed.all_reduce(sm, op=torch.distributed.ReduceOp.SUM)
+    return float(mx[0]), float(sm[0])
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -762,13 +775,7 @@ def main():
     replay_ok = bool(torch.equal(acc_rep, acc_rec))
     tokens = float((acc_rep[args.warmup:].double() + 1).sum())
     # whole job: tokens of all ranks over the slowest rank's time
-    t = torch.tensor([ms, tokens], dtype=torch.float64, device=dev)
-    if world > 1:
-        mx = t.clone()
-        torch.distributed.all_reduce(mx, op=torch.distributed.ReduceOp.MAX)
-        sm = t.clone()
-        torch.distributed.all_reduce(sm, op=torch.distributed.ReduceOp.SUM)
-        ms, tokens = float(mx[0]), float(sm[1])
+    ms, tokens = whole_job(ms, tokens, dev)
     value = tokens / (ms / 1000.0)
     ms_per_step = ms / args.steps
     mean_tpr = float((acc_rep[args.warmup:].double() + 1).mean())
@@ -820,13 +827,7 @@ def main():
         if not args.no_e2e:
             e_ms, e_acc, h2d, d2h = b.replay_e2e(rounds, args.warmup, temp)
             e_tokens = float((e_acc.double() + 1).sum())
-            if world > 1:
-                t = torch.tensor([e_ms, e_tokens], dtype=torch.float64, device=dev)
-                mx = t.clone()
-                torch.distributed.all_reduce(mx, op=torch.distributed.ReduceOp.MAX)
-                sm = t.clone()
-                torch.distributed.all_reduce(sm, op=torch.distributed.ReduceOp.SUM)
-                e_ms, e_tokens = float(mx[0]), float(sm[1])
+            e_ms, e_tokens = whole_job(e_ms, e_tokens, dev)
             out["e2e"] = {"value": round(e_tokens / (e_ms / 1000), 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                           "d2h_bytes_per_step": d2h, "ms_per_step": round(e_ms / args.steps, 5)}
         out["round_ms"] = b.round_distribution(rounds, args.warmup, temp)
