@@ -285,6 +285,14 @@ spec_status spec_read_kv(spec_model* m, int32_t layer, int32_t seq_id, int32_t t
  * to `out` (device or host).  Enqueued on `stream`. */
 spec_status spec_debug_logits(spec_model* m, float* out, int64_t max_elems, void* stream);
 
+/* Failure-path check without a fault: one device-side wait that nothing
+ * completes (a fresh mbarrier phase with no arrival), bounded like every wait of
+ * the library.  It runs out after budget_cycles SM clock cycles (1 ..
+ * 4000000000; ~2 s at 2 GHz is the library's own budget) and records
+ * SPEC_ERR_TIMEOUT in the model's status word, which the next spec_sync_status()
+ * returns and clears; the context stays usable.  Enqueued on `stream`. */
+spec_status spec_debug_wait_probe(spec_model* m, int64_t budget_cycles, void* stream);
+
 /* Timing aid for long contexts: give each sequence (host ids) lens_host[b]
  * cached tokens with pseudo-random bf16 K/V (a hash of seed and position, scaled
  * by `scale`), without running the model.  Attention time does not depend on

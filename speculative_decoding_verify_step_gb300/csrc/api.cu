@@ -1162,6 +1162,13 @@ spec_status spec_debug_logits(spec_model* m, float* out, int64_t max_elems, void
   return SPEC_OK;
 }
 
+spec_status spec_debug_wait_probe(spec_model* m, int64_t budget_cycles, void* stream) {
+  if (spec_status s = check_model(m)) return s;
+  if (budget_cycles < 1 || budget_cycles > 4000000000ll) return fail(SPEC_ERR_INVALID_ARG, "budget out of range");
+  CUDA_TRY(launch_wait_probe(m->status, (unsigned long long)budget_cycles, static_cast<cudaStream_t>(stream)));
+  return SPEC_OK;
+}
+
 spec_status spec_kv_fill_random(spec_model* m, int32_t n, const int32_t* seq_ids_host, const int32_t* lens_host,
                                 uint64_t seed, float scale, void* stream) {
   if (spec_status s = check_model(m)) return s;

@@ -84,13 +84,14 @@ SPEC_DEVICE_INLINE bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 
 // Bounded wait: returns false (and records SPEC_ERR_TIMEOUT) if the phase with
 // the given parity has not completed within the cycle budget.
-SPEC_DEVICE_INLINE bool mbar_wait(uint64_t* bar, uint32_t parity, int* status) {
+SPEC_DEVICE_INLINE bool mbar_wait(uint64_t* bar, uint32_t parity, int* status,
+                                  unsigned long long budget = kWaitBudgetCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = clock64();
   while (true) {
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (clock64() - t0 > kWaitBudgetCycles) {
+    if (clock64() - t0 > budget) {
       set_status(status, SPEC_ERR_TIMEOUT);
       return false;
     }

@@ -257,6 +257,8 @@ struct ResetParams {
   int max_pages;
 };
 cudaError_t launch_seq_reset(const ResetParams& p, cudaStream_t st);
+// One bounded wait that nothing completes: records SPEC_ERR_TIMEOUT after `budget` cycles.
+cudaError_t launch_wait_probe(int* status, unsigned long long budget, cudaStream_t st);
 cudaError_t launch_commit_all(const int32_t* seq_ids, int B, int W, int max_batch, int32_t* seq_len,
                               cudaStream_t st);
 cudaError_t launch_alloc_to_len(const int32_t* seq_ids, const int32_t* lens, int n, int relative, int32_t* seq_len,

@@ -185,6 +185,25 @@ cudaError_t launch_prepare(const PrepareParams& p, cudaStream_t st) {
   return launch_k(prepare_kernel, dim3(1), dim3(32), 0, st, p);
 }
 
+// A bounded wait that nothing completes: phase 0 of a fresh mbarrier needs one
+// arrival and none comes, so the wait runs out after `budget` SM cycles and
+// records SPEC_ERR_TIMEOUT -- the path every pipeline wait of the library takes
+// when its partner stalls, taken here on purpose and with nothing else in flight.
+__global__ void wait_probe_kernel(int* status, unsigned long long budget) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) (void)mbar_wait(&bar, 0, status, budget);
+}
+
+cudaError_t launch_wait_probe(int* status, unsigned long long budget, cudaStream_t st) {
+  wait_probe_kernel<<<1, 32, 0, st>>>(status, budget);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_seq_reset(const ResetParams& p, cudaStream_t st) {
   return launch_k(seq_reset_kernel, dim3(1), dim3(32), 0, st, p.seq_ids, p.n, p.seq_len, p.seq_npages, p.page_table,
                   p.free_bits, p.max_pages);

@@ -40,8 +40,8 @@ class spec_config(ctypes.Structure):
 
 EXPORTS = ["spec_model_create", "spec_model_destroy", "spec_model_set_weight", "spec_seq_reset", "spec_prefill",
            "spec_decode_step", "spec_verify_step", "spec_verify_tree_step", "spec_score", "spec_accept_probs",
-           "spec_accept_greedy", "spec_get_kv_state", "spec_read_kv", "spec_debug_logits", "spec_kv_fill_random",
-           "spec_sync_status", "spec_max_pages_per_seq", "spec_last_launch_count", "spec_last_error",
+           "spec_accept_greedy", "spec_get_kv_state", "spec_read_kv", "spec_debug_logits", "spec_debug_wait_probe",
+           "spec_kv_fill_random", "spec_sync_status", "spec_max_pages_per_seq", "spec_last_launch_count", "spec_last_error",
            "spec_set_profiling", "spec_read_profile", "spec_accept_greedy_noalloc", "spec_verify_ragged",
            "spec_adjust_probs", "spec_verify_tree_sampled", "spec_accept_tree_probs"]
 
@@ -81,6 +81,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "spec_get_kv_state": (I32, [P, I32, P, P, P]),
         "spec_read_kv": (I32, [P, I32, I32, I32, I32, P, P]),
         "spec_debug_logits": (I32, [P, P, I64, P]),
+        "spec_debug_wait_probe": (I32, [P, I64, P]),
         "spec_kv_fill_random": (I32, [P, I32, P, P, U64, F32, P]),
         "spec_sync_status": (I32, [P, P]),
         "spec_max_pages_per_seq": (I32, [P]),
@@ -305,6 +306,11 @@ class SpecModel:
         _check(_lib.spec_read_kv(self.handle, layer, seq_id, t0, n, ctypes.c_void_p(k.data_ptr()),
                                  ctypes.c_void_p(v.data_ptr())))
         return k.view(torch.float16), v.view(torch.float16)
+
+    def debug_wait_probe(self, budget_cycles: int) -> None:
+        """Enqueue one bounded device wait that nothing completes; the next
+        sync_status() raises SpecError with SPEC_ERR_TIMEOUT (6)."""
+        _check(_lib.spec_debug_wait_probe(self.handle, int(budget_cycles), _stream()))
 
     def debug_logits(self, rows: int) -> torch.Tensor:
         """Logits of the last forward ([rows, vocab] fp32, device)."""

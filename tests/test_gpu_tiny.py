@@ -287,6 +287,29 @@ def test_capacity_error_is_reported(tiny):
         m.close()
 
 
+def test_timeout_status_is_reported(tiny):
+    """A bounded device wait that nothing completes runs out (~1 ms here), records
+    SPEC_ERR_TIMEOUT for the host, and leaves the context usable."""
+    need_gpu()
+    from speculative_decoding_verify_step_gb300 import spec
+    w, _ = tiny
+    m = cuda_model(synth.TINY, w, max_batch=2, max_width=4, max_seq_len=128, num_pages=8)
+    try:
+        m.sync_status()
+        m.debug_wait_probe(2_000_000)
+        with pytest.raises(spec.SpecError) as e:
+            m.sync_status()
+        assert e.value.status == 6
+        m.sync_status()                          # cleared
+        m.seq_reset([0])
+        m.prefill([0], torch.zeros(1, 10, dtype=torch.int32).cuda(), [10])
+        m.sync_status()
+        with pytest.raises(spec.SpecError):
+            m.debug_wait_probe(0)                # budget out of range: refused on the host
+    finally:
+        m.close()
+
+
 def test_invalid_arguments(tiny):
     need_gpu()
     from speculative_decoding_verify_step_gb300 import spec
