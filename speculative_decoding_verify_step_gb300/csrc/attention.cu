@@ -505,16 +505,15 @@ cudaError_t launch_attention_hd(const CUtensorMap* tmK, const CUtensorMap* tmV, 
 
 cudaError_t launch_attention(const CUtensorMap* tmK, const CUtensorMap* tmV, const AttnParams& p, cudaStream_t st) {
   // The widest cluster (16, 8, 4, 2 or 1 CTAs per sequence and kv head) whose grid
-  // fits one CTA per SM, while that still gives at least 4; else the widest that
-  // fits two per SM.  Few sequences spread their pages over many SMs, many keep
-  // more pages per CTA (and fewer merges).  Measured: a 16-CTA cluster doubled up
-  // on SMs (B = 2) is 7% slower per round than an 8-CTA cluster alone on them.
+  // fits one CTA per SM while clusters of 8 still do, else the widest that fits two
+  // per SM.  Few sequences spread their pages over many SMs, many keep more pages
+  // per CTA (and fewer merges).  Measured per round: an 8-CTA cluster alone on its
+  // SMs beats a 16-CTA one doubled up at B = 2 (8 kv heads) by 7% at 1K cached
+  // tokens and 10% at 4K; from B = 3 doubling up wins at 4K tokens by 6-11% (B = 3,
+  // B = 4, 15-node trees) and ties at 1K.
+  const int per_sm = p.B * p.Hkv * 8 <= p.sm_count ? 1 : 2;
   int cs = 16;
-  while (cs > 1 && p.B * p.Hkv * cs > p.sm_count) cs >>= 1;
-  if (cs < 4) {
-    cs = 16;
-    while (cs > 1 && p.B * p.Hkv * cs > 2 * p.sm_count) cs >>= 1;
-  }
+  while (cs > 1 && p.B * p.Hkv * cs > per_sm * p.sm_count) cs >>= 1;
   if (p.hd == 128) {
     switch (cs) {
       case 16: return launch_attention_hd<128, 16>(tmK, tmV, p, st);
