@@ -92,9 +92,6 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32)
   const int n_cons = blockDim.x / 32 - 1;  // consumer warps: (row tile, key group) pairs
   const int grp = p.Hq / p.Hkv;
   constexpr int KT = 4 / KG;                // 16-key tiles of a page per consumer warp
-  // key-group partials go straight into the cluster merge while it stays small
-  // (CS * KG partials per row); above that each CTA first combines its own
-  constexpr bool kFoldKg = KG > 1 && CS * KG <= 16;
 
   // Sequence state and the cached pages were written by kernels that completed
   // before the QKV projection (this kernel's predecessor) passed its own
@@ -135,10 +132,7 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32)
   float* kg_o = part_l + kMaxRowTiles * 16;                  // [slots][16][HD] key-group partials
   float* kg_m = kg_o + kMaxKgSlots * 16 * HD;                // [slots][16]
   float* kg_l = kg_m + kMaxKgSlots * 16;
-  float* kg_w = kg_l + kMaxKgSlots * 16;                     // [rows][KG] combine weights
-  float* cm = kg_w + kMaxRowTiles * 16 * 4;                  // [rows] combined max, sum
-  float* cl = cm + kMaxRowTiles * 16;
-  static_assert((kMaxRowTiles * 16 * (HD + 2 + 4 + 2) + kMaxKgSlots * 16 * (HD + 2)) * 4 <=
+  static_assert((kMaxRowTiles * 16 * (HD + 2) + kMaxKgSlots * 16 * (HD + 2)) * 4 <=
                     kAttnStages * 2 * kPage * HD * 2,
                 "partials fit in the stage buffers");
 
@@ -364,57 +358,21 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32)
         l_dst[r] = valid[h] ? lrow[h] : 0.f;
       }
     }
-    if constexpr (KG > 1 && !kFoldKg) {
-    asm volatile("bar.sync 1, %0;" ::"r"(n_cons * 32) : "memory");
-    // combine the KG partials of every row: weights 2^(m_kg - max m), then O, m, l
-    const int n_rows_launch = (n_cons / KG) * 16;
-    const int ctid = threadIdx.x;  // consumer threads are 0 .. n_cons*32-1
-    for (int r = ctid; r < n_rows_launch; r += n_cons * 32) {
-      const int t = r / 16, rr = r % 16;
-      float mk[KG], mt = -INFINITY;
-#pragma unroll
-      for (int k = 0; k < KG; ++k) {
-        mk[k] = k == 0 ? part_m[r] : kg_m[(t * (KG - 1) + k - 1) * 16 + rr];
-        mt = fmaxf(mt, mk[k]);
-      }
-      float lt = 0.f;
-#pragma unroll
-      for (int k = 0; k < KG; ++k) {
-        const float wk = (mt == -INFINITY || mk[k] == -INFINITY) ? 0.f : fast_exp2(mk[k] - mt);
-        kg_w[r * 4 + k] = wk;
-        lt += wk * (k == 0 ? part_l[r] : kg_l[(t * (KG - 1) + k - 1) * 16 + rr]);
-      }
-      cm[r] = mt;
-      cl[r] = lt;
-    }
-    asm volatile("bar.sync 1, %0;" ::"r"(n_cons * 32) : "memory");
-    for (int e = ctid; e < n_rows_launch * HD; e += n_cons * 32) {
-      const int r = e / HD, d = e % HD;
-      const int t = r / 16, rr = r % 16;
-      float o = kg_w[r * 4] * part_o[e];
-#pragma unroll
-      for (int k = 1; k < KG; ++k) o += kg_w[r * 4 + k] * kg_o[((t * (KG - 1) + k - 1) * 16 + rr) * HD + d];
-      part_o[e] = o;
-      if (d == 0) {
-        part_m[r] = cm[r];
-        part_l[r] = cl[r];
-      }
-    }
-    }
   }
   // every CTA of the cluster has its partials in shared memory
   if (warp == n_cons) pdl_wait();  // every thread below may write the output
   cluster.sync();
   if (!s_fail) {
     // CTA `rank` merges rows rank, rank + CS, ...: each thread owns 4 consecutive
-    // output elements of one row and issues all of its remote loads -- the (m, l)
-    // of the row's partials and their 4 partial outputs -- before using any, so
-    // the merge costs one round trip over distributed shared memory.  The
-    // partials are the CS CTAs' (and, when folded, each CTA's KG key groups').
+    // output elements of one row.  The row's partials are the CS CTAs' key-group
+    // partials (KG per CTA); they are taken 16 at a time, and each batch's remote
+    // loads -- (m, l) and the 4 partial outputs of every partial -- are all issued
+    // before any is used, so the merge costs one distributed-shared-memory round
+    // trip per batch.  Across batches the running sums are rescaled to the new max.
     // out = sum_p 2^(m_p - max m) o_p / sum_p 2^(m_p - max m) l_p
     constexpr int V4 = HD / 4;
-    constexpr int KGM = kFoldKg ? KG : 1;  // key-group partials per CTA in the merge
-    constexpr int NP = CS * KGM;
+    constexpr int NP = CS * KG;                  // partials per row
+    constexpr int NB = NP < 16 ? NP : 16;        // partials per batch
     const int n_my_rows = rows > rank ? (rows - rank + CS - 1) / CS : 0;
     const uint32_t o_base = smem_u32(part_o), m_base = smem_u32(part_m), l_base = smem_u32(part_l);
     const uint32_t ko_base = smem_u32(kg_o), km_base = smem_u32(kg_m), kl_base = smem_u32(kg_l);
@@ -422,12 +380,14 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32)
       const int lr = it / V4, d4 = it % V4;
       const int r = rank + lr * CS;
       const int rtr = r / 16, rr = r % 16;
-      float ms[NP], ls[NP];
-      float4 os[NP];
+      float mrun = -INFINITY, den = 0.f, n0 = 0.f, n1 = 0.f, n2 = 0.f, n3 = 0.f;
 #pragma unroll
-      for (int s = 0; s < CS; ++s) {
+      for (int p0 = 0; p0 < NP; p0 += NB) {
+        float ms[NB], ls[NB];
+        float4 os[NB];
 #pragma unroll
-        for (int k = 0; k < KGM; ++k) {
+        for (int q = 0; q < NB; ++q) {
+          const int pi = p0 + q, s_ = pi / KG, k = pi % KG;  // partial pi: CTA s_, key group k
           uint32_t ma, la, oa;
           if (k == 0) {
             ma = m_base + r * 4;
@@ -439,23 +399,31 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32)
             la = kl_base + sl * 4;
             oa = ko_base + (sl * HD + d4 * 4) * 4;
           }
-          ms[s * KGM + k] = ld_dsmem_f32(mapa_u32(ma, s));
-          ls[s * KGM + k] = ld_dsmem_f32(mapa_u32(la, s));
-          os[s * KGM + k] = ld_dsmem_f4(mapa_u32(oa, s));
+          ms[q] = ld_dsmem_f32(mapa_u32(ma, s_));
+          ls[q] = ld_dsmem_f32(mapa_u32(la, s_));
+          os[q] = ld_dsmem_f4(mapa_u32(oa, s_));
         }
-      }
-      float mmax = -INFINITY;
+        float mb = mrun;
 #pragma unroll
-      for (int s = 0; s < NP; ++s) mmax = fmaxf(mmax, ms[s]);
-      float den = 0.f, n0 = 0.f, n1 = 0.f, n2 = 0.f, n3 = 0.f;
+        for (int q = 0; q < NB; ++q) mb = fmaxf(mb, ms[q]);
+        if (mb != -INFINITY && mrun != mb) {  // rescale the running sums to the new max
+          const float a = mrun == -INFINITY ? 0.f : fast_exp2(mrun - mb);
+          den *= a;
+          n0 *= a;
+          n1 *= a;
+          n2 *= a;
+          n3 *= a;
+        }
+        mrun = mb;
 #pragma unroll
-      for (int s = 0; s < NP; ++s) {
-        const float w = (mmax == -INFINITY || ms[s] == -INFINITY) ? 0.f : fast_exp2(ms[s] - mmax);
-        den += w * ls[s];
-        n0 += w * os[s].x;
-        n1 += w * os[s].y;
-        n2 += w * os[s].z;
-        n3 += w * os[s].w;
+        for (int q = 0; q < NB; ++q) {
+          const float w = (mb == -INFINITY || ms[q] == -INFINITY) ? 0.f : fast_exp2(ms[q] - mb);
+          den += w * ls[q];
+          n0 += w * os[q].x;
+          n1 += w * os[q].y;
+          n2 += w * os[q].z;
+          n3 += w * os[q].w;
+        }
       }
       const float inv = den > 0.f ? 1.f / den : 0.f;
       const int j = r / grp, hq = kvh * grp + r % grp;
