@@ -1227,6 +1227,12 @@ spec_status spec_sync_status(spec_model* m, void* stream) {
   int code = 0;
   CUDA_TRY(cudaMemcpy(&code, m->status, 4, cudaMemcpyDeviceToHost));
   CUDA_TRY(cudaMemset(m->status, 0, 4));
+  // The host's per-sequence length bounds (launch shapes only: attention split,
+  // key groups, L2 prefetch budget) grow by the window on every call; the stream
+  // is idle here, so take the exact lengths instead.
+  std::vector<int32_t> lens(m->cfg.max_batch);
+  CUDA_TRY(cudaMemcpy(lens.data(), m->seq_len, lens.size() * 4, cudaMemcpyDeviceToHost));
+  for (size_t i = 0; i < lens.size(); ++i) m->host_len_bound[i] = std::max(0, (int)lens[i]);
   if (code != 0) return fail((spec_status)code, "device reported status %d", code);
   return SPEC_OK;
 }
