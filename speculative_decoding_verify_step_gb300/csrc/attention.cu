@@ -15,15 +15,14 @@
 // K/V pages (64 tokens x head_dim fp16 per kv head) are streamed by TMA with
 // the 128-byte swizzle into a 3-stage mbarrier pipeline fed by one producer
 // warp.  Consumer warps are (row tile, key group) pairs: a warp owns 16 query
-// rows and 64/KG keys of every page, runs QK^T and PV on mma.sync with an online
-// softmax in fp32 (exp2 domain), and the KG partials of a row tile are combined
-// in shared memory at the end.  Splitting the keys of a page over KG warps puts
-// a warp on every scheduler, so the short dependent MMA chains of a 16-row tile
-// overlap instead of running back to back.  A sequence's pages are split over a
-// thread-block cluster of 1 to 16 CTAs (the widest whose grid fits one wave);
-// each CTA leaves its partial (unnormalised O,
-// running max, running sum) in its own shared memory and the cluster merges
-// them through distributed shared memory with log-sum-exp weights, so the
+// rows and 64/KG keys of every page and runs QK^T and PV on mma.sync with an
+// online softmax in fp32 (exp2 domain).  Splitting the keys of a page over KG
+// warps puts a warp on every scheduler, so the short dependent MMA chains of a
+// 16-row tile overlap instead of running back to back.  A sequence's pages are
+// split over a thread-block cluster of 1 to 16 CTAs (the widest whose grid fits
+// one wave); every warp leaves its partial (unnormalised O, running max, running
+// sum) in its CTA's shared memory and the cluster merges all CS x KG partials of
+// a row through distributed shared memory with log-sum-exp weights, so the
 // partials never go to HBM and no separate merge launch is needed.
 #include <cooperative_groups.h>
 #include <math.h>
@@ -53,8 +52,10 @@ constexpr int kMaxKgSlots = 3;        // partials of key groups > 0 (row tiles x
 
 // Key groups per page for a launch with `row_tiles` row tiles: four consumer warps
 // at most, so a CTA stays small enough for several to share an SM.  Splitting keys
-// pays off only when a CTA has pages enough to amortise the final combine (measured
-// on GB300: from about 4 pages per CTA with one row tile, 8 with two).
+// pays off only when a CTA has pages enough to amortise the extra partials in the
+// merge (measured on GB300: from about 4 pages per CTA with one row tile, 8 with
+// two; a four-way split at 2 pages and a two-way one at 2-3 pages were slower or
+// within noise).
 inline int key_groups(int row_tiles, int pages_per_cta) {
   if (row_tiles == 1 && pages_per_cta >= 4) return 4;
   if (row_tiles == 2 && pages_per_cta >= 8) return 2;
