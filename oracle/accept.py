@@ -22,7 +22,7 @@ Sources:
   ancestor mask; greedy acceptance keeps the longest root-to-leaf path whose
   tokens match the target argmax.
 
-Readings where the pages leave a step open (each is listed in the design doc):
+Readings where the pages leave a step open:
 * The test r_i < p/q is evaluated as fl32(u * q(x)) < p(x): no division, the
   same set of outcomes for q > 0; q(x) = 0 < p(x) accepts, p(x) = 0 rejects.
 * Uniforms u[b, 0..gamma-1] drive the tests, u[b, gamma] drives the one final

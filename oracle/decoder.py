@@ -16,7 +16,7 @@ page size the ninfer draft-depth sweep pins ("kPagedKVPageSize = 64").
 
 The decoder itself is never printed on the pages; the model is the standard
 Llama form the workload names (RMSNorm, RoPE, grouped-query attention, SwiGLU,
-untied embedding and LM head).  Readings (listed in the design doc):
+untied embedding and LM head).  Readings where the pages are silent:
 * RMSNorm: x / sqrt(mean(x^2) + eps) * g.
 * RoPE: half-split pairs (i, i + hd/2), inverse frequency theta^(-2i/hd),
   position = absolute token index (tree nodes: L + depth); cos/sin in float64.
