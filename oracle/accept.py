@@ -30,6 +30,9 @@ Readings where the pages leave a step open:
 * The final draw is an integer inverse CDF (see `draw_index`) so that it is
   reproducible bit for bit under any summation order.
 * Greedy ties go to the lowest token index.
+* A final draw whose target row has no mass on the 2^-40 grid at all (an input
+  that is not a distribution, e.g. an all-zero row given to the standalone
+  acceptance; a softmax row always has mass) returns token 0, chain and tree alike.
 * Sampling adjustments (`adjust_probs`): temperature first (in `target_probs`),
   then top-k, then top-p over the top-k renormalised distribution; rank order is
   p descending with the lower token index first on equal p; masses on the same
@@ -200,7 +203,9 @@ def accept_stochastic(p: np.ndarray, q: np.ndarray, x: np.ndarray, u: np.ndarray
 
     Returns (accepted [B], committed [B, W] (-1 padded), final [B], zero_residual [B])
     where zero_residual flags rounds whose residual had no mass on the 2^-40 grid;
-    those draw from p at the break row instead.
+    those draw from p at the break row instead.  A row of p with no mass on the
+    grid either (all zeros: not a distribution, so never a softmax row) gives
+    token 0.
     """
     p = np.asarray(p, dtype=np.float32)
     B, W, V = p.shape
@@ -225,6 +230,7 @@ def accept_stochastic(p: np.ndarray, q: np.ndarray, x: np.ndarray, u: np.ndarray
     zero = tok < 0
     if zero.any():
         tok[zero] = draw_index_rows(fixed_point_mass(p[bi[zero], n[zero]]), u[zero, gamma])
+    tok[tok < 0] = 0                             # p without mass: token 0
     committed = np.full((B, W), -1, dtype=np.int64)
     for b in range(B):
         committed[b, :n[b]] = x[b, :n[b]]

@@ -297,6 +297,36 @@ def test_zero_residual_falls_back_to_p():
     assert n[0] == 0 and zero[0] and tok[0] == 0      # floor(0.1*2^24)*S>>24 lands in token 0
 
 
+def test_massless_target_row_gives_token_0():
+    """A target row with no mass on the 2^-40 grid (all zeros, or every entry below
+    2^-40) is not a distribution; the draw returns token 0 by the stated reading,
+    in the chain (after a rejection, and as the bonus) and in the tree."""
+    V = 6
+    for row in (np.zeros(V, np.float32), np.full(V, 2.0 ** -42, np.float32)):
+        p = np.stack([row, row])[None]                                  # [1, 2, V]
+        q = np.full((1, 1, V), 1.0 / V, np.float32)
+        for u_last in (0.0, 0.37, 0.999):
+            u = np.array([[0.5, u_last]], np.float32)
+            n, com, tok, zero = A.accept_stochastic(p, q, np.array([[3]]), u)   # p(x) = 0: rejected
+            assert n[0] == 0 and zero[0] and tok[0] == 0 and com[0].tolist() == [0, -1]
+            n, com, tok, _ = A.accept_stochastic(p, q, np.array([[3]]), u,
+                                                 accept_fn=lambda u_, qx, px: np.ones_like(u_, bool))
+            assert n[0] == 1 and tok[0] == 0 and com[0].tolist() == [3, 0]
+            pt = np.stack([row, row])[None]
+            for qq in (None, np.full((1, 2, V), 1.0 / V, np.float32)):
+                acc, path, com, fin = A.accept_tree_stochastic(pt, qq, np.array([[1, 4]]), np.array([-1, 0]),
+                                                               np.array([[u_last, 0.5]], np.float32))
+                assert acc[0] == 0 and fin[0] == 0 and com[0, 0] == 0
+    # one token with grid mass is drawn whatever u is
+    row = np.zeros(V, np.float32)
+    row[4] = 2.0 ** -40
+    p = np.stack([row, row])[None]
+    for u_last in (0.0, 0.5, 0.999):
+        _, _, tok, _ = A.accept_stochastic(p, np.full((1, 1, V), 1.0 / V, np.float32), np.array([[3]]),
+                                           np.array([[0.5, u_last]], np.float32))
+        assert tok[0] == 4
+
+
 # -------------------------------------------------------------------- tree
 def _brute_tree(logits, tok, parent):
     N = len(parent)
