@@ -40,6 +40,8 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "accepted tok/s at Llama-8B shape; T_verify/T_decode for gamma+1=2..8; HBM GB/s"
+# the 15-node draft tree of the tree workload: root + 2 + 4 + 8 nodes (top-2 branching)
+TREE15 = [-1, 0, 0, 1, 1, 2, 2, 3, 3, 4, 4, 5, 5, 6, 6]
 UNIT = "accepted tok/s"
 
 
@@ -67,6 +69,11 @@ def parse_args():
                     help="profiler mode only: nucleus sampling on every row (adds the selection kernel)")
     ap.add_argument("--ncu", action="store_true",
                     help="profiler mode: cache filled directly (no prefill), fixed drafts, W + K verify rounds")
+    ap.add_argument("--tree", choices=["greedy", "sampled"], default=None,
+                    help="profiler mode: 15-node binary-tree verify rounds instead of chain rounds")
+    ap.add_argument("--isolated", action="store_true",
+                    help="profiler mode: the library's per-kernel profiling on (no cross-kernel L2 prefetch), "
+                         "as in the bench's roofline pass")
     return ap.parse_args()
 
 
@@ -482,7 +489,7 @@ class Bench:
                                    "achieved_GBps": round(by / (t / 1000) / 1e9, 1),
                                    "frac_of_peak": round(by / (t / 1000) / 1e9 / hbm_peak, 4)}
         out["long_context_b8_ctx32768"] = lc
-        tree = [-1, 0, 0, 1, 1, 2, 2, 3, 3, 4, 4, 5, 5, 6, 6]
+        tree = TREE15
         lens = [4096] * 4
         t_dec = self.timed_rounds(4, 1, lens, steps, warmup, temp=0.0)
         t = self.timed_rounds(4, len(tree), lens, steps, warmup, tree=tree)
@@ -736,14 +743,26 @@ def run_ncu_mode(args):
     ids = torch.arange(B, dtype=torch.int32, device=dev)
     g = torch.Generator(device=dev)
     g.manual_seed(3)
+    if args.tree:
+        W = len(TREE15)
     tok = torch.randint(0, V, (B, W), generator=g, device=dev).int()
-    q = synth.dirichlet1((B, W - 1, V), seed=4, device=dev).float()
+    q = synth.dirichlet1((B, W if args.tree else W - 1, V), seed=4, device=dev).float()
     u = synth.uniforms((B, W), seed=6, device=dev)
     outs = None
     torch.cuda.synchronize()
     tp = None if args.top_p is None else [args.top_p] * B
+    if args.isolated:
+        m.set_profiling(True)
     for _ in range(args.warmup + args.steps):
-        outs = m.verify_step(ids, tok, q=q, u=u, temperature=args.temperature, outs=outs, top_p=tp)
+        if args.tree == "greedy":
+            outs = m.verify_tree_step(ids, tok, TREE15, outs=outs)
+        elif args.tree == "sampled":
+            outs = m.verify_tree_sampled(ids, tok, TREE15, u, q=q, temperature=args.temperature, outs=outs,
+                                         top_p=tp)
+        else:
+            outs = m.verify_step(ids, tok, q=q, u=u, temperature=args.temperature, outs=outs, top_p=tp)
+        if args.isolated:
+            m.read_profile()
     torch.cuda.synchronize()
     m.sync_status()
     print(json.dumps({"ncu_mode": True, "layers": args.layers, "launches_per_round": m.last_launch_count(),

@@ -35,6 +35,12 @@
  *     offending memory accesses, so the context stays usable.
  *   - A sampled (temperature > 0) round with q or u missing is an error; the
  *     library never falls back to greedy.
+ *   - seq_ids of one call must be distinct and in 0..max_batch-1.  A call that
+ *     breaks this is refused on the device (status word SPEC_ERR_INVALID_ARG):
+ *     no KV is written and no sequence's length or pages change.  A sequence
+ *     whose window cannot get its KV pages (SPEC_ERR_CAPACITY) likewise keeps
+ *     its length and pages; the other sequences of the call commit normally.
+ *     Outputs of refused sequences are written but carry no meaning.
  *   - spec_last_error() gives a thread-local message for the last failure.
  */
 #ifndef SPEC_VERIFY_H
@@ -223,8 +229,13 @@ spec_status spec_score(spec_model* m, int32_t B, int32_t W, const int32_t* seq_i
 
 /* Standalone acceptance on given probabilities (no model): p [B, gamma+1, V]
  * fp32 target probabilities (row j = distribution after row j's token),
- * q [B, gamma, V], x [B, gamma] drafts, u [B, gamma+1].  Same decision code as
- * spec_verify_step; bit-exact by construction (fp32 products, integer CDF). */
+ * q [B, gamma, V], x [B, gamma] drafts, u [B, gamma+1].  Runs the acceptance
+ * kernel of spec_verify_step's sampled rounds (the same accept tests, residual
+ * and integer-CDF draw across an 8-CTA cluster), reading p from memory instead
+ * of deriving it from the LM head's logits; so its decisions on given p, q, u
+ * are those of the model round and match a sequential CPU computation bit for
+ * bit (fp32 products, integer CDF).  A row of p without mass on the 2^-40 grid
+ * (not a distribution) draws token 0. */
 spec_status spec_accept_probs(int32_t B, int32_t gamma, int32_t V, const float* p, const float* q,
                               const int32_t* x, const float* u, int32_t* accepted, int32_t* committed,
                               int32_t* bonus, void* stream);
@@ -265,7 +276,10 @@ spec_status spec_accept_greedy(int32_t B, int32_t gamma, int32_t V, const float*
  * current; make that first call before any stream capture.  All calls share the
  * one scratch array: calls that overlap on the GPU (different streams, no
  * ordering between them) race and give undefined results.  Each row's entry is
- * rewritten before it is read, so nothing needs clearing between calls. */
+ * rewritten before it is read, so nothing needs clearing between calls.  The
+ * looked-up address is kept for the life of the process: it assumes the device's
+ * primary context is never reset (cudaDeviceReset, or a context torn down and
+ * created again, would leave it stale). */
 spec_status spec_accept_greedy_noalloc(int32_t B, int32_t gamma, int32_t V, const float* logits,
                                        const int32_t* x, int32_t* accepted, int32_t* committed,
                                        int32_t* bonus, void* stream);
@@ -293,6 +307,17 @@ spec_status spec_debug_logits(spec_model* m, float* out, int64_t max_elems, void
  * returns and clears; the context stays usable.  Enqueued on `stream`. */
 spec_status spec_debug_wait_probe(spec_model* m, int64_t budget_cycles, void* stream);
 
+/* Give sequence seq_id (host int) exactly n_tokens cached tokens whose K and V
+ * are the caller's: k, v device [n_layers, n_tokens, n_kv_heads, head_dim] fp16
+ * bits (the cache's format), 16-byte aligned.  The sequence is emptied first,
+ * then gets pages for n_tokens slots (lowest free first) and the values copied
+ * in; its length becomes n_tokens, so the next call's row 0 is the pending
+ * token at position n_tokens.  Lets a test start the model and a reference
+ * from one cache without a prefill.  An exhausted pool sets SPEC_ERR_CAPACITY
+ * in the status word (length 0).  Synchronises `stream`. */
+spec_status spec_kv_write(spec_model* m, int32_t seq_id, int32_t n_tokens, const uint16_t* k, const uint16_t* v,
+                          void* stream);
+
 /* Timing aid for long contexts: give each sequence (host ids) lens_host[b]
  * cached tokens with pseudo-random bf16 K/V (a hash of seed and position, scaled
  * by `scale`), without running the model.  Attention time does not depend on
@@ -303,7 +328,8 @@ spec_status spec_kv_fill_random(spec_model* m, int32_t n, const int32_t* seq_ids
 /* Per-kernel timing for reports.  While enabled, every weight-streaming
  * projection launch and every attention launch of a forward is bracketed by CUDA
  * events on the call's stream (this serialises those launches; use it in a
- * separate measuring pass).  Classes: 0 QKV, 1 O, 2 gate/up, 3 down, 4 LM head,
+ * separate measuring pass), and no kernel prefetches the next kernel's weights
+ * into L2, so every launch is timed on the bytes it moves itself.  Classes: 0 QKV, 1 O, 2 gate/up, 3 down, 4 LM head,
  * 5 attention (+ merge).  spec_read_profile synchronises the device, adds the
  * recorded durations to ms[6] and launch counts to launches[6], and its
  * algorithmic HBM bytes (weights; K/V pages read) to bytes[6], then clears the

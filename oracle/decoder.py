@@ -261,6 +261,21 @@ class OracleDecoder:
             return logits, hid
         return logits
 
+    def load_cache(self, s: int, k: np.ndarray, v: np.ndarray):
+        """Start sequence s from a given cache: k, v [n_layers, n, n_kv, hd] become
+        its KV at slots 0..n-1 (pages taken lowest free first) and its length n.
+        The GPU path's counterpart receives the same values, so both sides attend
+        over one cache without a prefill."""
+        s = int(s)
+        n = int(k.shape[1])
+        self.kv.reset(s)
+        self.kv.ensure(s, n)
+        for t in range(n):
+            pg, off = self.kv.slot(s, t)
+            self.kv.k[:, pg, :, off] = k[:, t]
+            self.kv.v[:, pg, :, off] = v[:, t]
+        self.kv.truncate(s, n)
+
     # ------------------------------------------------------------------- rounds
     def prefill(self, seq_ids, prompts):
         """Write KV for prompt[:-1] of each sequence (lengths may differ); the last

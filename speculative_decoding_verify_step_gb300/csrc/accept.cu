@@ -15,7 +15,10 @@
 // whose running sum exceeds t.  Integer sums do not depend on the reduction
 // order, so the draw is reproducible bit for bit against a sequential CPU
 // computation on the same probabilities.  If the residual has no mass on that
-// grid the draw falls back to p at the same row.
+// grid the draw falls back to p at the same row; a row of p without mass on the
+// grid (not a distribution: only given probabilities can be one) gives token 0.
+// The round kernel below takes these decisions for model rounds (from the LM
+// head's tile statistics) and for given probabilities (standalone entry point).
 //
 // Tree (section 10.3): walk from the root to the child whose token equals the
 // argmax at the current node (lowest node index on ties), then move the
@@ -23,6 +26,7 @@
 #include <cooperative_groups.h>
 #include <math.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "kvstate.cuh"
@@ -145,127 +149,56 @@ SPEC_DEVICE_INLINE unsigned long long block_exscan_u64(unsigned long long v, uns
   return pre;
 }
 
-template <bool SAMPLED, PSource SRC>
-__global__ void __launch_bounds__(kAccThreads) accept_chain_kernel(const __grid_constant__ AcceptParams p) {
-  __shared__ int s_n, s_tok, s_zero;
-  __shared__ unsigned long long s_scan[33];
+// Standalone greedy acceptance: one block per sequence takes the argmax of its
+// W rows (or reads them from row_argmax), then the longest matching prefix.
+__global__ void __launch_bounds__(kAccThreads) accept_greedy_kernel(const __grid_constant__ AcceptParams p) {
+  __shared__ int s_n, s_tok;
+  __shared__ int s_am[kMaxWidth];
+  __shared__ ArgMax s_red[32];
   pdl_wait();
   pdl_launch_dependents();
   const int b = blockIdx.x;
   const int W = p.gamma + 1;
   const int V = p.V;
   const long long row0 = (long long)b * W;
-
-  auto xdraft = [&](int i) -> int { return p.tok[(long long)b * p.tok_stride + p.tok_offset + i - 1]; };
-  auto prob = [&](int row, int v) -> float {
-    const float* r = p.rows + (row0 + row) * V;
-    if constexpr (SRC == PSource::kProbs) {
-      return r[v];
-    } else {
-      return expf((r[v] - p.row_max[row0 + row]) * p.inv_temp) / p.row_sum[row0 + row];
-    }
-  };
-
-  // Standalone greedy acceptance has no row-statistics pass: take the argmax of
-  // the W rows here (lowest index on ties).
-  __shared__ int s_am[kMaxWidth];
-  __shared__ ArgMax s_red[32];
-  if constexpr (!SAMPLED) {
-    if (p.row_argmax == nullptr) {
-      const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-      for (int row = 0; row < W; ++row) {
-        const float* r = p.rows + (row0 + row) * V;
-        ArgMax best{-INFINITY, 0x7fffffff};
-        for (int v = threadIdx.x; v < V; v += kAccThreads) best = better(best, ArgMax{r[v], v});
-        best = warp_argmax(best);
-        if (lane == 0) s_red[warp] = best;
-        __syncthreads();
-        if (warp == 0) {
-          ArgMax a = lane < kAccThreads / 32 ? s_red[lane] : ArgMax{-INFINITY, 0x7fffffff};
-          a = warp_argmax(a);
-          if (lane == 0) s_am[row] = a.i == 0x7fffffff ? 0 : a.i;
-        }
-        __syncthreads();
+  auto xdraft = [&](int i) -> int { return p.tok[(long long)b * p.gamma + i - 1]; };
+  if (p.row_argmax == nullptr) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int row = 0; row < W; ++row) {
+      const float* r = p.rows + (row0 + row) * V;
+      ArgMax best{-INFINITY, 0x7fffffff};
+      for (int v = threadIdx.x; v < V; v += kAccThreads) best = better(best, ArgMax{r[v], v});
+      best = warp_argmax(best);
+      if (lane == 0) s_red[warp] = best;
+      __syncthreads();
+      if (warp == 0) {
+        ArgMax a = lane < kAccThreads / 32 ? s_red[lane] : ArgMax{-INFINITY, 0x7fffffff};
+        a = warp_argmax(a);
+        if (lane == 0) s_am[row] = a.i == 0x7fffffff ? 0 : a.i;
       }
+      __syncthreads();
     }
   }
   auto am = [&](int row) -> int { return p.row_argmax ? p.row_argmax[row0 + row] : s_am[row]; };
-
   if (threadIdx.x < 32) {
-    const int n = accepted_prefix(p.gamma, threadIdx.x, p.status, [&](int i) -> int {
+    const int n = accepted_prefix(p.gamma, threadIdx.x, nullptr, [&](int i) -> int {
       const int x = xdraft(i);
       if (x < 0 || x >= V) return -1;
-      if constexpr (SAMPLED) {
-        const float qx = p.q[((long long)b * p.gamma + (i - 1)) * V + x];
-        return __fmul_rn(p.u[row0 + i - 1], qx) < prob(i - 1, x) ? 1 : 0;
-      } else {
-        return x == am(i - 1) ? 1 : 0;
-      }
+      return x == am(i - 1) ? 1 : 0;
     });
     if (threadIdx.x == 0) {
       s_n = n;
-      s_zero = 0;
-      if constexpr (!SAMPLED) s_tok = am(n);
+      s_tok = am(n);
     }
   }
   __syncthreads();
   const int n = s_n;
-
-  if constexpr (SAMPLED) {
-    const bool rejected = n < p.gamma;
-    const float* qn = rejected ? p.q + ((long long)b * p.gamma + n) * V : nullptr;
-    const int chunk = (V + kAccThreads - 1) / kAccThreads;
-    const int v0 = min(V, threadIdx.x * chunk), v1 = min(V, v0 + chunk);
-    const float uf = p.u[row0 + p.gamma];
-    const unsigned long long m = (unsigned long long)floorf(uf * 16777216.0f);
-    for (int pass = 0; pass < 2; ++pass) {
-      const bool use_resid = rejected && pass == 0;
-      auto mass = [&](int v) -> unsigned long long {
-        const float pv = prob(n, v);
-        const float r = use_resid ? fmaxf(0.f, pv - qn[v]) : pv;
-        return (unsigned long long)floorf(r * 1099511627776.0f);  // r * 2^40, exact
-      };
-      unsigned long long local = 0;
-      for (int v = v0; v < v1; ++v) local += mass(v);
-      unsigned long long S;
-      const unsigned long long pre = block_exscan_u64(local, s_scan, &S);
-      if (S == 0ull) {
-        if (threadIdx.x == 0) s_zero = 1;
-        if (!use_resid) {  // p itself has no mass on the grid: cannot happen for a distribution
-          if (threadIdx.x == 0) s_tok = 0;
-          break;
-        }
-        continue;  // fall back to p at the break row
-      }
-      // t = floor(m * S / 2^24) with a 128-bit product (m < 2^24, S < 2^58)
-      const unsigned long long hi = __umul64hi(m, S), lo = m * S;
-      const unsigned long long t = (hi << 40) | (lo >> 24);
-      if (local > 0 && pre <= t && t < pre + local) {
-        unsigned long long run = pre;
-        for (int v = v0; v < v1; ++v) {
-          run += mass(v);
-          if (run > t) {
-            s_tok = v;
-            break;
-          }
-        }
-      }
-      break;
-    }
-    __syncthreads();
-  }
   const int tok_final = s_tok;
   for (int j = threadIdx.x; j < W; j += kAccThreads)
     p.committed[row0 + j] = j < n ? xdraft(j + 1) : (j == n ? tok_final : -1);
   if (threadIdx.x == 0) {
     p.accepted[b] = n;
     p.bonus[b] = tok_final;
-    if (p.seq_ids) {
-      const int s = p.seq_ids[b];
-      if (s >= 0 && s < p.max_batch)
-        truncate_seq(s, min(p.seq_len[s] + 1 + n, p.max_pages * kPage), p.seq_len, p.seq_npages, p.page_table,
-                     p.max_pages, p.free_bits);
-    }
   }
 }
 
@@ -312,7 +245,12 @@ SPEC_DEVICE_INLINE void merge_row_stats(const RoundAcceptParams& p, long long m,
 // One verify round's acceptance and commit for sequence blockIdx.y.  Sampled
 // rounds run as a cluster of kDrawCluster CTAs that split the vocabulary for
 // the final draw; greedy rounds use one CTA.
-template <bool SAMPLED>
+//
+// SRC = kProbs: the same acceptance on given target probabilities (p.probs, rows
+// of sequence b at b * (gamma + 1)) and drafts p.x, without a commit -- the
+// standalone entry point, so that this kernel's decisions can be checked on
+// identical inputs.
+template <bool SAMPLED, PSource SRC = PSource::kLogits>
 __global__ void __launch_bounds__(kAccThreads) accept_round_kernel(const __grid_constant__ RoundAcceptParams p) {
   __shared__ float s_max[kMaxWidth], s_z[kMaxWidth];
   __shared__ int s_am[kMaxWidth];
@@ -324,19 +262,21 @@ __global__ void __launch_bounds__(kAccThreads) accept_round_kernel(const __grid_
   const int b = blockIdx.y;
   const int V = p.V;
   const int Wmax = p.gamma + 1;                  // stride of u and committed
-  const int Wfwd = p.seq_wlen[b];                // rows the forward scored for this sequence
+  const int Wfwd = p.seq_wlen ? p.seq_wlen[b] : Wmax;  // rows the forward scored for this sequence
   const int W = p.cap ? max(1, min(p.cap[b], Wfwd)) : Wfwd;  // rows the acceptance may use
   const int gamma = W - 1;
-  const long long row0 = p.seq_rowoff[b];
+  const long long row0 = p.seq_rowoff ? p.seq_rowoff[b] : (long long)b * Wmax;
   const long long urow = (long long)b * Wmax;
   const int warp = threadIdx.x >> 5;
 
-  if (warp < W) merge_row_stats(p, row0 + warp, SAMPLED, &s_max[warp], &s_z[warp], &s_am[warp]);
-  __syncthreads();
+  if constexpr (SRC == PSource::kLogits) {
+    if (warp < W) merge_row_stats(p, row0 + warp, SAMPLED, &s_max[warp], &s_z[warp], &s_am[warp]);
+    __syncthreads();
+  }
   // top-k / top-p: the selection kernel's statistics and kept set of each row
   __shared__ SelRow s_sel[kMaxWidth];
   __shared__ double s_inv[kMaxWidth];
-  const bool adjust = SAMPLED && p.sel != nullptr;
+  const bool adjust = SAMPLED && SRC == PSource::kLogits && p.sel != nullptr;
   if (adjust) {
     if (threadIdx.x < W) {
       const long long r = row0 + threadIdx.x;
@@ -349,10 +289,16 @@ __global__ void __launch_bounds__(kAccThreads) accept_round_kernel(const __grid_
   }
 
   auto prob = [&](int row, int v) -> float {
-    const float pv = prob_from_logit(p.logits[(row0 + row) * V + v], s_max[row], p.inv_temp, s_z[row]);
-    return adjust ? adjusted_prob(pv, v, s_sel[row], s_inv[row]) : pv;
+    if constexpr (SRC == PSource::kProbs) {
+      return p.probs[(row0 + row) * V + v];
+    } else {
+      const float pv = prob_from_logit(p.logits[(row0 + row) * V + v], s_max[row], p.inv_temp, s_z[row]);
+      return adjust ? adjusted_prob(pv, v, s_sel[row], s_inv[row]) : pv;
+    }
   };
-  auto xdraft = [&](int i) -> int { return p.tok[row0 + i]; };  // x_i = window row i
+  auto xdraft = [&](int i) -> int {  // x_i = window row i, or the given drafts
+    return p.x ? p.x[(long long)b * p.gamma + i - 1] : p.tok[row0 + i];
+  };
 
   if (warp == 0) {
     const int n = accepted_prefix(gamma, threadIdx.x, p.status, [&](int i) -> int {
@@ -374,7 +320,9 @@ __global__ void __launch_bounds__(kAccThreads) accept_round_kernel(const __grid_
     for (int j = 0; j < Wmax; ++j) p.committed[urow + j] = j < n ? xdraft(j + 1) : (j == n ? tok_final : -1);
     p.accepted[b] = n;
     p.bonus[b] = tok_final;
-    if (p.seq_ids) {
+    // a sequence whose window was refused (bad or repeated id, no pages) keeps
+    // its length and pages
+    if (p.seq_ids && (!p.seq_ok || p.seq_ok[b])) {
       const int s = p.seq_ids[b];
       if (s >= 0 && s < p.max_batch)
         truncate_seq(s, min(p.seq_len[s] + 1 + n, p.max_pages * kPage), p.seq_len, p.seq_npages, p.page_table,
@@ -453,7 +401,9 @@ __global__ void __launch_bounds__(kAccThreads) accept_round_kernel(const __grid_
 // depths run in order with a barrier between them.
 SPEC_DEVICE_INLINE void commit_tree_path(const TreeParams& p, int b, const int* path, int n, int tok_final) {
   const int s = p.seq_ids[b];
-  const bool ok = s >= 0 && s < p.max_batch;  // a bad id was flagged by the prepare kernel
+  // a refused window (bad or repeated id, no pages; flagged by the prepare kernel)
+  // moves no KV and keeps the sequence's length and pages
+  const bool ok = s >= 0 && s < p.max_batch && (!p.seq_ok || p.seq_ok[b]);
   const int L = ok ? p.seq_len[s] : 0;
   const int vec_per_head = p.hd / 8;  // 16-byte vectors
   const int per_tok = p.n_layers * p.Hkv * vec_per_head;
@@ -746,17 +696,35 @@ cudaError_t launch_row_stats(const float* rows, int n_rows, int V, float inv_tem
                   argmax, row_max, row_sum);
 }
 
-cudaError_t launch_accept_chain(const AcceptParams& p, bool sampled, PSource src, cudaStream_t st) {
-  dim3 grid(p.B), block(kAccThreads);
-  if (!sampled) return launch_k(accept_chain_kernel<false, PSource::kLogits>, grid, block, 0, st, p);
-  if (src == PSource::kProbs) return launch_k(accept_chain_kernel<true, PSource::kProbs>, grid, block, 0, st, p);
-  return launch_k(accept_chain_kernel<true, PSource::kLogits>, grid, block, 0, st, p);
+cudaError_t launch_accept_greedy(const AcceptParams& p, cudaStream_t st) {
+  return launch_k(accept_greedy_kernel, dim3(p.B), dim3(kAccThreads), 0, st, p);
 }
 
 cudaError_t launch_accept_round(const RoundAcceptParams& p, bool sampled, cudaStream_t st) {
   if (!sampled) return launch_k(accept_round_kernel<false>, dim3(1, p.B), dim3(kAccThreads), 0, st, p);
   return launch_k_cluster(accept_round_kernel<true>, dim3(kDrawCluster, p.B), dim3(kAccThreads), 0, st,
                           dim3(kDrawCluster, 1, 1), p);
+}
+
+cudaError_t launch_accept_round_probs(const RoundAcceptParams& p, cudaStream_t st) {
+  // one cluster per sequence along grid y (at most 65535): larger batches in chunks
+  constexpr int kChunk = 65535;
+  const int W = p.gamma + 1;
+  for (int b0 = 0; b0 < p.B; b0 += kChunk) {
+    RoundAcceptParams c = p;
+    c.B = std::min(kChunk, p.B - b0);
+    c.probs = p.probs + (long long)b0 * W * p.V;
+    if (p.q) c.q = p.q + (long long)b0 * p.gamma * p.V;
+    if (p.x) c.x = p.x + (long long)b0 * p.gamma;
+    c.u = p.u + (long long)b0 * W;
+    c.accepted = p.accepted + b0;
+    c.committed = p.committed + (long long)b0 * W;
+    c.bonus = p.bonus + b0;
+    cudaError_t e = launch_k_cluster(accept_round_kernel<true, PSource::kProbs>, dim3(kDrawCluster, c.B),
+                                     dim3(kAccThreads), 0, st, dim3(kDrawCluster, 1, 1), c);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t launch_accept_tree_sampled(const TreeParams& p, cudaStream_t st) {
@@ -841,16 +809,13 @@ extern "C" spec_status spec_accept_greedy_noalloc(int32_t B, int32_t gamma, int3
     ap.B = B;
     ap.gamma = gamma;
     ap.V = V;
-    ap.inv_temp = 1.f;
     ap.rows = logits;
     ap.tok = x;
-    ap.tok_stride = gamma;
-    ap.tok_offset = 0;
     ap.row_argmax = scratch;
     ap.accepted = accepted;
     ap.committed = committed;
     ap.bonus = bonus;
-    e = launch_accept_chain(ap, false, PSource::kLogits, st);
+    e = launch_accept_greedy(ap, st);
   }
   if (e != cudaSuccess) {
     record_error(cudaGetErrorString(e));

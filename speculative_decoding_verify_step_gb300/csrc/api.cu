@@ -123,6 +123,7 @@ struct spec_model {
   float *sel_max = nullptr, *sel_z = nullptr;
   int32_t *row_pos = nullptr, *row_slot = nullptr, *seq_start = nullptr;
   int32_t *seq_wlen = nullptr, *seq_rowoff = nullptr;  // per-call window layout (prepare kernel)
+  int32_t* seq_ok = nullptr;  // per-call: 1 = the window got its pages and may commit
   float *rope_cos = nullptr, *rope_sin = nullptr;
   int32_t *scratch_ids = nullptr, *scratch_ids2 = nullptr, *scratch_tok = nullptr, *scratch_lens = nullptr;
   int32_t *scratch_acc = nullptr, *scratch_bonus = nullptr;
@@ -229,6 +230,7 @@ spec_status forward(spec_model* m, int B, int W, const int32_t* seq_ids, const i
   pp.row_pos = m->row_pos;
   pp.row_slot = m->row_slot;
   pp.seq_start = m->seq_start;
+  pp.seq_ok = m->seq_ok;
   pp.tok = tok;
   pp.vocab = c.vocab;
   pp.status = m->status;
@@ -278,10 +280,13 @@ spec_status forward(spec_model* m, int B, int W, const int32_t* seq_ids, const i
   // bytes beyond the attention's own K/V: that much of the O projection's and
   // then the gate/up projection's weights is prefetched into L2 (none once the
   // K/V reads alone fill the attention's time).
-  const double pf = std::max(0.0, kAttnL2Budget - kv_bytes);
+  // While per-kernel profiling is on, no kernel prefetches another's weights: each
+  // launch is then timed on the bytes it moves itself.
+  const bool prefetch = !m->profiling;
+  const double pf = prefetch ? std::max(0.0, kAttnL2Budget - kv_bytes) : 0.0;
   const unsigned long long pf_o = (unsigned long long)std::min(pf, wb_o) & ~15ull;
   const unsigned long long pf_gu = (unsigned long long)std::max(0.0, std::min(pf - (double)pf_o, wb_gu)) & ~15ull;
-  const double proj_pf = BM <= 16 ? kProjL2Budget : 0.0;
+  const double proj_pf = prefetch && BM <= 16 ? kProjL2Budget : 0.0;
   for (int l = 0; l < c.n_layers; ++l) {
     auto& Ly = m->layers[l];
     ap.l2_next[0] = Ly.wo;
@@ -396,13 +401,16 @@ RoundAcceptParams round_params(spec_model* m, int B, int gamma, const int32_t* s
   r.tstat_sum = m->tstat_sum;
   r.tstat_arg = m->tstat_arg;
   r.tstat_stride = m->M_max;
+  r.probs = nullptr;
   r.q = q;
   r.tok = tok;
+  r.x = nullptr;
   r.u = u;
   r.accepted = accepted;
   r.committed = committed;
   r.bonus = bonus;
   r.seq_ids = seq_ids;
+  r.seq_ok = m->seq_ok;
   r.seq_len = m->seq_len;
   r.seq_npages = m->seq_npages;
   r.page_table = m->page_table;
@@ -592,6 +600,7 @@ spec_status spec_model_create(const spec_config* cfg, spec_model** out) {
   ALLOC(m->seq_start, c.max_batch);
   ALLOC(m->seq_wlen, c.max_batch);
   ALLOC(m->seq_rowoff, c.max_batch);
+  ALLOC(m->seq_ok, c.max_batch);
   ALLOC(m->rope_cos, (size_t)c.max_seq_len * (hd / 2));
   ALLOC(m->rope_sin, (size_t)c.max_seq_len * (hd / 2));
   ALLOC(m->scratch_ids, c.max_batch);
@@ -792,7 +801,7 @@ spec_status spec_prefill(spec_model* m, int32_t B, const int32_t* seq_ids, const
     CUDA_TRY(launch_gather_tokens(tokens, stride, m->scratch_lens, k, c0, W, m->scratch_tok, seq_ids, m->scratch_ids2,
                                   st));
     if (auto s = forward(m, k, W, m->scratch_ids2, m->scratch_tok, depth, anc, false, false, 1.f, st)) return s;
-    CUDA_TRY(launch_commit_all(m->scratch_ids2, k, W, m->cfg.max_batch, m->seq_len, st));
+    CUDA_TRY(launch_commit_all(m->scratch_ids2, m->seq_ok, k, W, m->cfg.max_batch, m->seq_len, st));
   }
   for (int i = 0; i < B; ++i) {  // the ragged tail of each prompt
     const int n_cache = lens_host[perm[i]] - 1;
@@ -803,7 +812,7 @@ spec_status spec_prefill(spec_model* m, int32_t B, const int32_t* seq_ids, const
     CUDA_TRY(launch_gather_tokens(tokens, stride, m->scratch_lens + i, 1, c0, r, m->scratch_tok, seq_ids,
                                   m->scratch_ids2, st));
     if (auto s = forward(m, 1, r, m->scratch_ids2, m->scratch_tok, depth, anc, false, false, 1.f, st)) return s;
-    CUDA_TRY(launch_commit_all(m->scratch_ids2, 1, r, m->cfg.max_batch, m->seq_len, st));
+    CUDA_TRY(launch_commit_all(m->scratch_ids2, m->seq_ok, 1, r, m->cfg.max_batch, m->seq_len, st));
   }
   m->last_launches = g_launch_count;
   // host bound: sequences ids are on the device; raise every slot's bound
@@ -824,6 +833,7 @@ TreeParams tree_params(spec_model* m, int B, int n_nodes, const int32_t* seq_ids
   tp.committed = committed;
   tp.bonus = bonus;
   tp.seq_ids = seq_ids;
+  tp.seq_ok = m->seq_ok;
   tp.seq_len = m->seq_len;
   tp.seq_npages = m->seq_npages;
   tp.page_table = m->page_table;
@@ -995,30 +1005,8 @@ spec_status spec_verify_tree_step(spec_model* m, int32_t B, int32_t n_nodes, con
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   g_launch_count = 0;
   if (auto s = forward(m, B, n_nodes, seq_ids, tok, depth, anc, true, false, 1.f, st)) return s;
-  TreeParams tp{};
-  tp.B = B;
-  tp.N = n_nodes;
+  TreeParams tp = tree_params(m, B, n_nodes, seq_ids, tok, parent_host, accepted, committed, bonus);
   tp.stats = round_params(m, B, n_nodes - 1, seq_ids, tok, nullptr, nullptr, 1.f, accepted, committed, bonus);
-  tp.V = m->cfg.vocab;
-  for (int j = 0; j < 16; ++j) tp.parent[j] = j < n_nodes ? parent_host[j] : -1;
-  tp.tok = tok;
-  tp.accepted = accepted;
-  tp.committed = committed;
-  tp.bonus = bonus;
-  tp.seq_ids = seq_ids;
-  tp.seq_len = m->seq_len;
-  tp.seq_npages = m->seq_npages;
-  tp.page_table = m->page_table;
-  tp.free_bits = m->free_bits;
-  tp.max_pages = m->max_pages;
-  tp.max_batch = m->cfg.max_batch;
-  tp.kpool = m->kpool;
-  tp.vpool = m->vpool;
-  tp.n_layers = m->cfg.n_layers;
-  tp.num_pages = m->cfg.num_pages;
-  tp.Hkv = m->cfg.n_kv_heads;
-  tp.hd = m->cfg.head_dim;
-  tp.status = m->status;
   CUDA_TRY(launch_accept_tree(tp, st));
   bump_bounds(m, n_nodes);
   m->last_launches = g_launch_count;
@@ -1030,21 +1018,20 @@ spec_status spec_accept_probs(int32_t B, int32_t gamma, int32_t V, const float* 
   if (B < 1 || gamma < 0 || gamma + 1 > kMaxWidth || V < 1) return fail(SPEC_ERR_INVALID_ARG, "bad shape");
   if (!p || !u || (gamma > 0 && (!q || !x)) || !accepted || !committed || !bonus)
     return fail(SPEC_ERR_INVALID_ARG, "NULL argument");
-  AcceptParams ap{};
-  ap.B = B;
-  ap.gamma = gamma;
-  ap.V = V;
-  ap.inv_temp = 1.f;
-  ap.rows = p;
-  ap.q = q;
-  ap.tok = x;
-  ap.tok_stride = gamma;
-  ap.tok_offset = 0;
-  ap.u = u;
-  ap.accepted = accepted;
-  ap.committed = committed;
-  ap.bonus = bonus;
-  CUDA_TRY(launch_accept_chain(ap, true, PSource::kProbs, static_cast<cudaStream_t>(stream)));
+  // the model round's acceptance kernel, reading the given probabilities
+  RoundAcceptParams rp{};
+  rp.B = B;
+  rp.gamma = gamma;
+  rp.V = V;
+  rp.inv_temp = 1.f;
+  rp.probs = p;
+  rp.q = q;
+  rp.x = x;
+  rp.u = u;
+  rp.accepted = accepted;
+  rp.committed = committed;
+  rp.bonus = bonus;
+  CUDA_TRY(launch_accept_round_probs(rp, static_cast<cudaStream_t>(stream)));
   return SPEC_OK;
 }
 
@@ -1101,16 +1088,13 @@ spec_status spec_accept_greedy(int32_t B, int32_t gamma, int32_t V, const float*
   ap.B = B;
   ap.gamma = gamma;
   ap.V = V;
-  ap.inv_temp = 1.f;
   ap.rows = logits;
   ap.tok = x;
-  ap.tok_stride = gamma;
-  ap.tok_offset = 0;
-  ap.row_argmax = nullptr;  // argmax computed inside the accept kernel
+  ap.row_argmax = nullptr;  // argmax taken inside the accept kernel
   ap.accepted = accepted;
   ap.committed = committed;
   ap.bonus = bonus;
-  CUDA_TRY(launch_accept_chain(ap, false, PSource::kLogits, static_cast<cudaStream_t>(stream)));
+  CUDA_TRY(launch_accept_greedy(ap, static_cast<cudaStream_t>(stream)));
   return SPEC_OK;
 }
 
@@ -1189,6 +1173,31 @@ spec_status spec_kv_fill_random(spec_model* m, int32_t n, const int32_t* seq_ids
                                 st));
   CUDA_TRY(cudaStreamSynchronize(st));
   for (int i = 0; i < n; ++i) m->host_len_bound[seq_ids_host[i]] = lens_host[i];
+  return SPEC_OK;
+}
+
+spec_status spec_kv_write(spec_model* m, int32_t seq_id, int32_t n_tokens, const uint16_t* k, const uint16_t* v,
+                          void* stream) {
+  if (spec_status s = check_model(m)) return s;
+  const spec_config& c = m->cfg;
+  if (seq_id < 0 || seq_id >= c.max_batch) return fail(SPEC_ERR_INVALID_ARG, "sequence id %d out of range", seq_id);
+  if (n_tokens < 0 || n_tokens > c.max_seq_len) return fail(SPEC_ERR_CAPACITY, "n_tokens %d outside 0..max_seq_len", n_tokens);
+  if (n_tokens > 0 && (!k || !v)) return fail(SPEC_ERR_INVALID_ARG, "NULL argument");
+  if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15u)
+    return fail(SPEC_ERR_INVALID_ARG, "k and v must be 16-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t ids[1] = {seq_id}, lens[1] = {n_tokens};
+  CUDA_TRY(cudaMemcpyAsync(m->scratch_ids, ids, 4, cudaMemcpyHostToDevice, st));
+  CUDA_TRY(cudaMemcpyAsync(m->scratch_lens, lens, 4, cudaMemcpyHostToDevice, st));
+  ResetParams rp{m->scratch_ids, 1, m->seq_len, m->seq_npages, m->page_table, m->free_bits, m->max_pages};
+  CUDA_TRY(launch_seq_reset(rp, st));
+  CUDA_TRY(launch_alloc_to_len(m->scratch_ids, m->scratch_lens, 1, 0, m->seq_len, m->seq_npages, m->page_table,
+                               m->free_bits, m->max_pages, c.num_pages, c.max_batch, m->status, st));
+  CUDA_TRY(launch_kv_write(m->kpool, m->vpool, m->page_table, m->max_pages, seq_id, n_tokens,
+                           reinterpret_cast<const act_t*>(k), reinterpret_cast<const act_t*>(v), c.n_layers,
+                           c.num_pages, c.n_kv_heads, c.head_dim, st));
+  CUDA_TRY(cudaStreamSynchronize(st));  // ids and lens are host buffers
+  m->host_len_bound[seq_id] = n_tokens;
   return SPEC_OK;
 }
 

@@ -47,8 +47,8 @@ SPEC_DEVICE_INLINE float fast_exp2(float x) {
 
 constexpr int kAttnStages = 3;
 constexpr int kMaxRowTiles = 4;       // up to 64 query rows (W * group) per CTA
-constexpr int kMaxConsumerWarps = 4;  // row tiles x key groups
-constexpr int kMaxKgSlots = 3;        // partials of key groups > 0 (row tiles x (KG - 1))
+constexpr int kMaxConsumerWarps = 8;  // row tiles x key groups
+constexpr int kMaxKgSlots = 6;        // partials of key groups > 0 (row tiles x (KG - 1))
 
 // Key groups per page for a launch with `row_tiles` row tiles: four consumer warps
 // at most, so a CTA stays small enough for several to share an SM.  Splitting keys

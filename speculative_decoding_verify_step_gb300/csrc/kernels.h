@@ -117,6 +117,7 @@ struct PrepareParams {
   int32_t* row_pos;         // [B*W]
   int32_t* row_slot;        // [B*W] physical slot (page*64 + off) or -1
   int32_t* seq_start;       // [B]
+  int32_t* seq_ok;          // [B] out: 1 = the window got its pages and may commit
   const int32_t* tok;       // [B*W] token ids to validate
   int vocab;
   int* status;
@@ -125,32 +126,19 @@ cudaError_t launch_prepare(const PrepareParams& p, cudaStream_t st);
 
 enum class PSource { kLogits = 0, kProbs = 1 };
 
+// Standalone greedy acceptance on given logits (no model, no commit).
 struct AcceptParams {
   int B, gamma, V;
-  float inv_temp;           // 1/T for sampled rounds
-  const float* rows;        // [B*W, V] logits or probabilities
-  const float* q;           // [B, gamma, V] (sampled) or null
-  const int32_t* tok;       // [B, W] window tokens (x_i = tok[b, i]) -- or drafts when x_stride == gamma
-  int tok_stride, tok_offset;
-  const float* u;           // [B, W] (sampled) or null
-  const int32_t* row_argmax;  // [B*W] (greedy)
-  const float* row_max;     // [B*W] (sampled, logits)
-  const float* row_sum;     // [B*W] (sampled, logits)
-  int32_t* accepted;        // [B]
-  int32_t* committed;       // [B, W]
-  int32_t* bonus;           // [B]
-  // commit (null seq_ids = no commit)
-  const int32_t* seq_ids;
-  int32_t* seq_len;
-  int32_t* seq_npages;
-  int32_t* page_table;
-  uint32_t* free_bits;
-  int max_pages, max_batch;
-  int* status;
+  const float* rows;          // [B*W, V] logits
+  const int32_t* tok;         // [B, gamma] drafts
+  const int32_t* row_argmax;  // [B*W] argmax of each row, or null: taken inside the kernel
+  int32_t* accepted;          // [B]
+  int32_t* committed;         // [B, W]
+  int32_t* bonus;             // [B]
 };
 cudaError_t launch_row_stats(const float* rows, int n_rows, int V, float inv_temp, bool sampled, int32_t* argmax,
                              float* row_max, float* row_sum, cudaStream_t st);
-cudaError_t launch_accept_chain(const AcceptParams& p, bool sampled, PSource src, cudaStream_t st);
+cudaError_t launch_accept_greedy(const AcceptParams& p, cudaStream_t st);
 
 // Acceptance of a model round from the LM head's per-tile statistics.
 constexpr int kDrawCluster = 8;
@@ -158,8 +146,8 @@ constexpr int kMaxDrawCluster = 16;
 struct SelRow;
 struct RoundAcceptParams {
   int B, gamma, V;           // gamma: the widest window - 1 (stride of q, u, committed)
-  const int32_t* seq_wlen;   // [B] window rows of sequence b
-  const int32_t* seq_rowoff; // [B] first flat row of sequence b
+  const int32_t* seq_wlen;   // [B] window rows of sequence b (null: gamma + 1 each)
+  const int32_t* seq_rowoff; // [B] first flat row of sequence b (null: b * (gamma + 1))
   const int32_t* cap;        // [B] acceptance cap (verify length) or null
   float inv_temp;
   const float* logits;       // [B*W, V]
@@ -168,13 +156,16 @@ struct RoundAcceptParams {
   const float* tstat_sum;
   const int32_t* tstat_arg;
   int tstat_stride;
+  const float* probs;        // [B*W, V] given target probabilities (PSource::kProbs)
   const float* q;            // [B, gamma, V] (sampled)
   const int32_t* tok;        // [rows] window tokens, sequence b at seq_rowoff[b]
+  const int32_t* x;          // [B, gamma] drafts (standalone) or null: x_i = window row i
   const float* u;            // [B, gamma+1] (sampled)
   int32_t* accepted;
   int32_t* committed;        // [B, W]
   int32_t* bonus;
   const int32_t* seq_ids;    // null: no commit
+  const int32_t* seq_ok;     // [B] from the prepare kernel: 0 = leave the sequence as it was
   int32_t* seq_len;
   int32_t* seq_npages;
   int32_t* page_table;
@@ -187,6 +178,8 @@ struct RoundAcceptParams {
   const float* sel_z;
 };
 cudaError_t launch_accept_round(const RoundAcceptParams& p, bool sampled, cudaStream_t st);
+// Sampled acceptance of given probabilities (p.probs, p.x; no commit) by the same kernel.
+cudaError_t launch_accept_round_probs(const RoundAcceptParams& p, cudaStream_t st);
 
 // ---------------------------------------------------------------- top-k / top-p
 constexpr int kSelCluster = 8;             // CTAs per probability row
@@ -225,6 +218,7 @@ struct TreeParams {
   int32_t* committed;        // [B, N]
   int32_t* bonus;
   const int32_t* seq_ids;
+  const int32_t* seq_ok;     // [B] from the prepare kernel: 0 = no KV move, no commit
   int32_t* seq_len;
   int32_t* seq_npages;
   int32_t* page_table;
@@ -259,8 +253,13 @@ struct ResetParams {
 cudaError_t launch_seq_reset(const ResetParams& p, cudaStream_t st);
 // One bounded wait that nothing completes: records SPEC_ERR_TIMEOUT after `budget` cycles.
 cudaError_t launch_wait_probe(int* status, unsigned long long budget, cudaStream_t st);
-cudaError_t launch_commit_all(const int32_t* seq_ids, int B, int W, int max_batch, int32_t* seq_len,
-                              cudaStream_t st);
+cudaError_t launch_commit_all(const int32_t* seq_ids, const int32_t* seq_ok, int B, int W, int max_batch,
+                              int32_t* seq_len, cudaStream_t st);
+// Sequence seq_id gets pages for n slots (lowest free first; it must be empty) and
+// the given K/V ([n_layers][n][Hkv][hd] fp16 each) copied into them; length n.
+cudaError_t launch_kv_write(__half* kpool, __half* vpool, const int32_t* page_table, int max_pages, int seq_id, int n,
+                            const __half* k, const __half* v, int n_layers, int num_pages, int Hkv, int hd,
+                            cudaStream_t st);
 cudaError_t launch_alloc_to_len(const int32_t* seq_ids, const int32_t* lens, int n, int relative, int32_t* seq_len,
                                 int32_t* seq_npages, int32_t* page_table, uint32_t* free_bits, int max_pages,
                                 int num_pages, int max_batch, int* status, cudaStream_t st);

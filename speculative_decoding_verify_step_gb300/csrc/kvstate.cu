@@ -12,10 +12,37 @@ namespace {
 // One warp.  Sequences are served in batch order b = 0..B-1 (deterministic page
 // assignment).  Sequence b owns flat rows rowoff_b .. rowoff_b + W_b - 1; for its
 // window row j: position L + depth[j] (RoPE), KV slot L + j.
+//
+// A batch that names a sequence id out of range, or the same id twice, is refused
+// as a whole (SPEC_ERR_INVALID_ARG): no page is taken, no KV slot is given out and
+// every seq_ok[b] is 0, so the commit leaves every sequence as it was (two windows
+// of one sequence would write the same slots and race on its length and pages).
+// A sequence whose window cannot get its pages (SPEC_ERR_CAPACITY) gives back the
+// pages this call took for it and gets seq_ok[b] = 0.
+constexpr int kMaxBatchWords = 4096 / 32;  // max_batch <= 4096
 __global__ void __launch_bounds__(32) prepare_kernel(const __grid_constant__ PrepareParams p) {
+  __shared__ uint32_t s_seen[kMaxBatchWords];
   pdl_wait();
   pdl_launch_dependents();
   const int lane = threadIdx.x;
+  for (int i = lane; i < kMaxBatchWords; i += 32) s_seen[i] = 0u;
+  __syncwarp();
+  bool bad_ids = false;
+  for (int b0 = 0; b0 < p.B; b0 += 32) {
+    const int b = b0 + lane;
+    bool bad = false;
+    if (b < p.B) {
+      const int s = p.seq_ids[b];
+      if (s < 0 || s >= p.max_batch) {
+        bad = true;
+      } else {
+        const uint32_t bit = 1u << (s & 31);
+        bad = (atomicOr(&s_seen[s >> 5], bit) & bit) != 0u;  // seen before: a repeat
+      }
+    }
+    bad_ids |= __any_sync(0xffffffffu, bad);
+  }
+  if (bad_ids && lane == 0) set_status(p.status, SPEC_ERR_INVALID_ARG);
   int off = 0;
   for (int b = 0; b < p.B; ++b) {
     const int s = p.seq_ids[b];
@@ -25,16 +52,15 @@ __global__ void __launch_bounds__(32) prepare_kernel(const __grid_constant__ Pre
       Wb = max(0, min(min(Wb, p.W), p.total_rows - off));
     }
     const bool sid_ok = s >= 0 && s < p.max_batch;
-    int L = 0;
-    bool ok = sid_ok;
-    if (!sid_ok) {
-      if (lane == 0) set_status(p.status, SPEC_ERR_INVALID_ARG);
-    } else {
-      L = p.seq_len[s];
+    const int L = sid_ok ? p.seq_len[s] : 0;
+    bool ok = sid_ok && !bad_ids;
+    if (ok) {
       if (L + Wb > p.max_seq_len) {
         ok = false;
       } else {
+        const int npg0 = p.seq_npages[s];
         ok = warp_ensure_pages(s, L + Wb, p.seq_npages, p.page_table, p.max_pages, p.free_bits, p.num_pages);
+        if (!ok && lane == 0) release_pages_from(s, npg0, p.seq_npages, p.page_table, p.max_pages, p.free_bits);
       }
       if (!ok && lane == 0) set_status(p.status, SPEC_ERR_CAPACITY);
     }
@@ -42,6 +68,7 @@ __global__ void __launch_bounds__(32) prepare_kernel(const __grid_constant__ Pre
       p.seq_start[b] = L;
       p.seq_wlen[b] = Wb;
       p.seq_rowoff[b] = off;
+      p.seq_ok[b] = ok ? 1 : 0;
     }
     for (int j = lane; j < Wb; j += 32) {
       const int m = off + j;
@@ -69,14 +96,15 @@ __global__ void seq_reset_kernel(const int32_t* seq_ids, int n, int32_t* seq_len
   for (int i = 0; i < n; ++i) truncate_seq(seq_ids[i], 0, seq_len, seq_npages, page_table, max_pages, free_bits);
 }
 
-// Prefill windows commit every row: L <- L + W.
-__global__ void commit_all_kernel(const int32_t* seq_ids, int B, int W, int max_batch, int32_t* seq_len) {
+// Prefill windows commit every row: L <- L + W (refused windows: unchanged).
+__global__ void commit_all_kernel(const int32_t* seq_ids, const int32_t* seq_ok, int B, int W, int max_batch,
+                                  int32_t* seq_len) {
   pdl_wait();
   pdl_launch_dependents();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= B) return;
   const int s = seq_ids[b];
-  if (s >= 0 && s < max_batch) seq_len[s] += W;
+  if (s >= 0 && s < max_batch && seq_ok[b]) seq_len[s] += W;
 }
 
 // Pages for each listed sequence, in list order (lowest free page first).
@@ -138,6 +166,28 @@ __global__ void kv_fill_kernel(act_t* kpool, act_t* vpool, const int32_t* page_t
   }
 }
 
+// Copy caller-supplied K/V of sequence seq_id (tokens 0..n-1, [n_layers][n][Hkv][hd]
+// fp16 each) into its pages.  grid: (pages of the sequence, n_layers); one block
+// per (page, layer), 16-byte vectors.
+__global__ void kv_write_kernel(act_t* kpool, act_t* vpool, const int32_t* page_table, int max_pages, int seq_id,
+                                int n, const act_t* k, const act_t* v, int num_pages, int Hkv, int hd) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int pi = blockIdx.x, layer = blockIdx.y;
+  const int pg = page_table[(long long)seq_id * max_pages + pi];
+  if (pg < 0) return;
+  const int vec = hd / 8;
+  const int t0 = pi * kPage;
+  const int nt = min(kPage, n - t0);
+  for (int e = threadIdx.x; e < nt * Hkv * vec; e += blockDim.x) {
+    const int d8 = e % vec, h = (e / vec) % Hkv, t = e / (vec * Hkv);
+    const long long src = (((long long)layer * n + t0 + t) * Hkv + h) * hd;
+    const long long dst = ((((long long)layer * num_pages + pg) * Hkv + h) * kPage + t) * hd;
+    reinterpret_cast<uint4*>(kpool + dst)[d8] = reinterpret_cast<const uint4*>(k + src)[d8];
+    reinterpret_cast<uint4*>(vpool + dst)[d8] = reinterpret_cast<const uint4*>(v + src)[d8];
+  }
+}
+
 __global__ void gather_tokens_kernel(const int32_t* tokens, int stride, const int32_t* perm, int k, int col0, int W,
                                      int32_t* out, const int32_t* seq_ids, int32_t* ids_out) {
   pdl_wait();
@@ -170,6 +220,15 @@ cudaError_t launch_gather_tokens(const int32_t* tokens, int stride, const int32_
                                  int32_t* out, const int32_t* seq_ids, int32_t* ids_out, cudaStream_t st) {
   return launch_k(gather_tokens_kernel, dim3(k), dim3(32), 0, st, tokens, stride, perm, k, col0, W, out, seq_ids,
                   ids_out);
+}
+
+cudaError_t launch_kv_write(act_t* kpool, act_t* vpool, const int32_t* page_table, int max_pages, int seq_id, int n,
+                            const act_t* k, const act_t* v, int n_layers, int num_pages, int Hkv, int hd,
+                            cudaStream_t st) {
+  const int pages = (n + kPage - 1) / kPage;
+  if (pages == 0) return cudaSuccess;
+  return launch_k(kv_write_kernel, dim3(pages, n_layers), dim3(256), 0, st, kpool, vpool, page_table, max_pages,
+                  seq_id, n, k, v, num_pages, Hkv, hd);
 }
 
 cudaError_t launch_init_state(int32_t* seq_len, int32_t* seq_npages, int32_t* page_table, uint32_t* free_bits,
@@ -209,9 +268,10 @@ cudaError_t launch_seq_reset(const ResetParams& p, cudaStream_t st) {
                   p.free_bits, p.max_pages);
 }
 
-cudaError_t launch_commit_all(const int32_t* seq_ids, int B, int W, int max_batch, int32_t* seq_len,
-                              cudaStream_t st) {
-  return launch_k(commit_all_kernel, dim3((B + 127) / 128), dim3(128), 0, st, seq_ids, B, W, max_batch, seq_len);
+cudaError_t launch_commit_all(const int32_t* seq_ids, const int32_t* seq_ok, int B, int W, int max_batch,
+                              int32_t* seq_len, cudaStream_t st) {
+  return launch_k(commit_all_kernel, dim3((B + 127) / 128), dim3(128), 0, st, seq_ids, seq_ok, B, W, max_batch,
+                  seq_len);
 }
 
 cudaError_t launch_alloc_to_len(const int32_t* seq_ids, const int32_t* lens, int n, int relative, int32_t* seq_len,

@@ -58,11 +58,9 @@ SPEC_DEVICE_INLINE bool warp_ensure_pages(int s, int upto, int32_t* seq_npages, 
   return ok;
 }
 
-// Set the cached length of sequence s and free every page whose first slot is
-// >= new_len.  Single thread.
-SPEC_DEVICE_INLINE void truncate_seq(int s, int new_len, int32_t* seq_len, int32_t* seq_npages, int32_t* page_table,
-                                     int max_pages, uint32_t* free_bits) {
-  const int keep = (new_len + kPage - 1) / kPage;
+// Return pages keep.. of sequence s to the pool (page table entries -1).  Single thread.
+SPEC_DEVICE_INLINE void release_pages_from(int s, int keep, int32_t* seq_npages, int32_t* page_table, int max_pages,
+                                           uint32_t* free_bits) {
   const int npg = seq_npages[s];
   for (int i = keep; i < npg; ++i) {
     const int pg = page_table[(long long)s * max_pages + i];
@@ -70,6 +68,13 @@ SPEC_DEVICE_INLINE void truncate_seq(int s, int new_len, int32_t* seq_len, int32
     page_table[(long long)s * max_pages + i] = -1;
   }
   if (npg > keep) seq_npages[s] = keep;
+}
+
+// Set the cached length of sequence s and free every page whose first slot is
+// >= new_len.  Single thread.
+SPEC_DEVICE_INLINE void truncate_seq(int s, int new_len, int32_t* seq_len, int32_t* seq_npages, int32_t* page_table,
+                                     int max_pages, uint32_t* free_bits) {
+  release_pages_from(s, (new_len + kPage - 1) / kPage, seq_npages, page_table, max_pages, free_bits);
   seq_len[s] = new_len;
 }
 

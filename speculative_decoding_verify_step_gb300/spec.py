@@ -43,7 +43,7 @@ EXPORTS = ["spec_model_create", "spec_model_destroy", "spec_model_set_weight", "
            "spec_accept_greedy", "spec_get_kv_state", "spec_read_kv", "spec_debug_logits", "spec_debug_wait_probe",
            "spec_kv_fill_random", "spec_sync_status", "spec_max_pages_per_seq", "spec_last_launch_count", "spec_last_error",
            "spec_set_profiling", "spec_read_profile", "spec_accept_greedy_noalloc", "spec_verify_ragged",
-           "spec_adjust_probs", "spec_verify_tree_sampled", "spec_accept_tree_probs"]
+           "spec_adjust_probs", "spec_verify_tree_sampled", "spec_accept_tree_probs", "spec_kv_write"]
 
 RAGGED_CAP_ACCEPT, RAGGED_COMPACT = 1, 2
 
@@ -83,6 +83,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "spec_debug_logits": (I32, [P, P, I64, P]),
         "spec_debug_wait_probe": (I32, [P, I64, P]),
         "spec_kv_fill_random": (I32, [P, I32, P, P, U64, F32, P]),
+        "spec_kv_write": (I32, [P, I32, I32, P, P, P]),
         "spec_sync_status": (I32, [P, P]),
         "spec_max_pages_per_seq": (I32, [P]),
         "spec_last_launch_count": (I32, [P]),
@@ -287,6 +288,16 @@ class SpecModel:
                                else None, _ptr(logits_out), _stream()))
         return logits_out
 
+    def kv_write(self, seq_id: int, k: torch.Tensor, v: torch.Tensor):
+        """Give sequence seq_id the cached K/V k, v: [n_layers, n_tokens, n_kv_heads,
+        head_dim] (converted to fp16, the cache's format); its length becomes n_tokens."""
+        want = (self.dims.n_layers, k.shape[1], self.dims.n_kv_heads, self.dims.head_dim)
+        if tuple(k.shape) != want or tuple(v.shape) != want:
+            raise ValueError(f"k, v must be {want}")
+        kk = k.to(device=self.device, dtype=torch.float16).contiguous()
+        vv = v.to(device=self.device, dtype=torch.float16).contiguous()
+        _check(_lib.spec_kv_write(self.handle, int(seq_id), int(k.shape[1]), _ptr(kk), _ptr(vv), _stream()))
+
     def kv_fill_random(self, seq_ids: Sequence[int], lens: Sequence[int], seed: int = 0, scale: float = 0.5):
         _check(_lib.spec_kv_fill_random(self.handle, len(seq_ids), _i32_host(seq_ids), _i32_host(lens), seed,
                                         scale, _stream()))
@@ -399,6 +410,9 @@ def spec_accept_greedy_noalloc(logits: torch.Tensor, x: Optional[torch.Tensor], 
         outs = (torch.empty(B, dtype=torch.int32, device=dev), torch.empty(B, W, dtype=torch.int32, device=dev),
                 torch.empty(B, dtype=torch.int32, device=dev))
     acc, com, bon = outs
+    for t, shape, what in ((acc, (B,), "accepted"), (com, (B, W), "committed"), (bon, (B,), "bonus")):
+        if t.dtype != torch.int32 or t.device != dev or tuple(t.shape) != shape:
+            raise ValueError(f"{what} must be an int32 tensor of shape {shape} on {dev}")
     xx = None if x is None else _dev_i32(x, dev)
     lg = logits.float().contiguous()
     _check(lib.spec_accept_greedy_noalloc(B, W - 1, V, _ptr(lg), _ptr(xx), _ptr(acc), _ptr(com), _ptr(bon),

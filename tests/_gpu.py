@@ -43,9 +43,10 @@ def greedy_clear(ref_logits, n_ref, margin=1e-2):
     return np.array([(gap[b, :n_ref[b] + 1] > margin).all() for b in range(B)])
 
 
-def stochastic_margin(p, q, x, u, n, margin=1e-2):
+def stochastic_margin(p, q, x, u, n, margin=1e-2, draw_margin=1e-4):
     """Clear when every accept test the round took has |u - p/q| > margin and the final
-    draw's threshold t sits more than margin*S from each CDF step edge."""
+    draw's threshold t sits more than margin x (its step's width) and more than
+    draw_margin x S from each edge of its CDF step."""
     B, W, V = p.shape
     clear = np.ones(B, bool)
     for b in range(B):
@@ -63,14 +64,15 @@ def stochastic_margin(p, q, x, u, n, margin=1e-2):
             clear[b] = False
             continue
         # the chosen step [C_{v-1}, C_v) of the integer CDF: t must sit more than
-        # margin x (step width) inside it, and more than 1e-4 S from either edge
-        # (the CDF drift that logit differences of the tolerance's size can cause)
+        # margin x (step width) inside it, and more than draw_margin x S from either
+        # edge (the CDF drift that logit differences can cause: 1e-4 S for logits of
+        # std ~0.3, up to ~1e-2 S for logits of std ~5)
         t = np.floor(float(u[b, W - 1]) * 2 ** 24) * S / 2 ** 24
         edges = np.cumsum(R)
         v = int(np.searchsorted(edges, t, side="right"))
         lo = edges[v - 1] if v > 0 else 0.0
         hi = edges[v]
         gapd = min(t - lo, hi - t)
-        if gapd <= margin * (hi - lo) or gapd <= 1e-4 * S:
+        if gapd <= margin * (hi - lo) or gapd <= draw_margin * S:
             clear[b] = False
     return clear

@@ -58,6 +58,28 @@ def test_accept_probs_bitexact(B, gamma, V, kw):
     np.testing.assert_array_equal(bon.cpu().numpy(), tok_ref)
 
 
+def test_accept_probs_massless_rows_give_token_0():
+    """Rows of p without mass on the 2^-40 grid (all zeros, or every entry below
+    2^-40) are not distributions; the draw gives token 0, as the oracle does, both
+    after a rejection and as the bonus.  V = 128256 spans the 8-CTA cluster."""
+    need_gpu()
+    from speculative_decoding_verify_step_gb300 import spec
+    for V in (1024, 128256):
+        p, q, x, u = _case(6, 3, V, seed=77)
+        p[0] = 0.0                                   # every row: rejected (p(x) = 0), then no mass
+        p[1, 3] = 0.0                                # the bonus row only
+        p[2] = np.float32(2.0 ** -42)                # mass below the grid everywhere
+        p[3, 1:] = 0.0
+        u[1, :3] = 0.0                               # sequence 1 accepts its drafts where p(x) > 0
+        n_ref, com_ref, tok_ref, _ = A.accept_stochastic(p, q, x, u)
+        d = lambda a: torch.from_numpy(a).cuda()
+        acc, com, bon = spec.spec_accept_probs(d(p), d(q), d(x), d(u))
+        np.testing.assert_array_equal(acc.cpu().numpy(), n_ref)
+        np.testing.assert_array_equal(com.cpu().numpy(), com_ref)
+        np.testing.assert_array_equal(bon.cpu().numpy(), tok_ref)
+        assert tok_ref[0] == 0 and tok_ref[2] == 0
+
+
 def test_accept_probs_exercise3_law():
     """Exercise 3 through the GPU rule: over a grid of uniforms the output frequencies
     equal p = (0.5, 0.3, 0.2) to the grid resolution."""

@@ -79,6 +79,26 @@ def test_standalone_bit_exact(V, tree, iid):
         assert (com[:, dmax:] == -1).all()
 
 
+def test_standalone_massless_rows_give_token_0():
+    """Target rows without mass on the 2^-40 grid draw token 0, as in the oracle."""
+    need_gpu()
+    spec = _spec()
+    parent = TREES["binary7"]
+    for V in (1024, 128256):
+        for iid in (True, False):
+            p, q, tok, u = _inputs(4, parent, V, iid, seed=91)
+            p[0] = 0.0
+            p[1, 1:] = np.float32(2.0 ** -42)
+            p[2, 0] = 0.0
+            n_ref, path, com_ref, fin_ref = A.accept_tree_stochastic(p, q if iid else None, tok, np.array(parent), u)
+            d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+            acc, com, bon = spec.spec_accept_tree_probs(d(p), d(q) if iid else None, d(tok), parent, d(u))
+            np.testing.assert_array_equal(acc.cpu().numpy(), n_ref)
+            np.testing.assert_array_equal(bon.cpu().numpy(), fin_ref)
+            np.testing.assert_array_equal(com.cpu().numpy()[:, :com_ref.shape[1]], com_ref)
+            assert fin_ref[0] == 0
+
+
 def test_chain_tree_equals_chain_acceptance():
     """parent[c] = c - 1: the tree kernel takes the chain kernel's decisions."""
     need_gpu()
