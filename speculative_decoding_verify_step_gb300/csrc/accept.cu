@@ -204,19 +204,30 @@ __global__ void __launch_bounds__(kAccThreads) accept_greedy_kernel(const __grid
 
 // Merge the LM head's per-128-column statistics of window row `row`: row max,
 // lowest index attaining it, and Z = sum_v exp((l_v - max) / T).  One warp per row;
-// fixed loop and shuffle order, so Z is reproducible.
+// lane l takes tiles l, l + 32, ... in ascending order, with eight tiles' loads in
+// flight at a time (the loads do not depend on each other), then a fixed shuffle
+// tree: the same order on every run, so Z is reproducible.
 SPEC_DEVICE_INLINE void merge_row_stats(const RoundAcceptParams& p, long long m, bool sampled, float* out_max,
                                         float* out_z, int* out_arg) {
+  constexpr int U = 8;
   const int lane = threadIdx.x & 31;
   float mx = -INFINITY;
   int am = 0x7fffffff;
-  for (int t = lane; t < p.n_tiles; t += 32) {
-    const float v = p.tstat_max[(long long)t * p.tstat_stride + m];
-    const int a = p.tstat_arg[(long long)t * p.tstat_stride + m];
-    if (v > mx || (v == mx && a < am)) {
-      mx = v;
-      am = a;
+  for (int t0 = lane; t0 < p.n_tiles; t0 += 32 * U) {
+    float v[U];
+    int a[U];
+#pragma unroll
+    for (int k = 0; k < U; ++k) {
+      const int t = t0 + 32 * k;
+      v[k] = t < p.n_tiles ? p.tstat_max[(long long)t * p.tstat_stride + m] : -INFINITY;
+      a[k] = t < p.n_tiles ? p.tstat_arg[(long long)t * p.tstat_stride + m] : 0x7fffffff;
     }
+#pragma unroll
+    for (int k = 0; k < U; ++k)
+      if (v[k] > mx || (v[k] == mx && a[k] < am)) {
+        mx = v[k];
+        am = a[k];
+      }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -229,9 +240,17 @@ SPEC_DEVICE_INLINE void merge_row_stats(const RoundAcceptParams& p, long long m,
   }
   float z = 0.f;
   if (sampled) {
-    for (int t = lane; t < p.n_tiles; t += 32) {
-      const float tm = p.tstat_max[(long long)t * p.tstat_stride + m];
-      z += p.tstat_sum[(long long)t * p.tstat_stride + m] * expf((tm - mx) * p.inv_temp);
+    for (int t0 = lane; t0 < p.n_tiles; t0 += 32 * U) {
+      float tm[U], ts[U];
+#pragma unroll
+      for (int k = 0; k < U; ++k) {
+        const int t = t0 + 32 * k;
+        tm[k] = t < p.n_tiles ? p.tstat_max[(long long)t * p.tstat_stride + m] : 0.f;
+        ts[k] = t < p.n_tiles ? p.tstat_sum[(long long)t * p.tstat_stride + m] : 0.f;
+      }
+#pragma unroll
+      for (int k = 0; k < U; ++k)
+        if (t0 + 32 * k < p.n_tiles) z += ts[k] * expf((tm[k] - mx) * p.inv_temp);
     }
     z = warp_sum(z);
   }

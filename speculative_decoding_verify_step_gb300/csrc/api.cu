@@ -250,6 +250,7 @@ spec_status forward(spec_model* m, int B, int W, const int32_t* seq_ids, const i
   base.inv_d = 1.f / d;
   base.eps = c.rms_eps;
   base.status = m->status;
+  base.sm_count = m->sm_count;
 
   AttnParams ap{};
   ap.q = m->qrot;

@@ -66,15 +66,17 @@ SPEC_DEVICE_INLINE void named_sync() {
 }
 
 // Rows [r_lo, r_hi) of the token tile that this CTA finishes: all of them, or with
-// split-K the share of split blockIdx.y.
+// split-K the share of split blockIdx.y of the tile's real rows (a ragged tile of 80
+// rows over 8 splits: 10 rows each, not 16 rows for five of them).
 template <int ROWS>
 SPEC_DEVICE_INLINE void tile_rows(const EpiParams& p, int m0, int& r_lo, int& r_hi) {
+  const int rows = min(ROWS, p.M - m0);
   r_lo = 0;
-  r_hi = min(ROWS, p.M - m0);
+  r_hi = rows;
   if (p.splits > 1) {
-    const int per = (ROWS + p.splits - 1) / p.splits;
-    r_lo = min(ROWS, (int)blockIdx.y * per);
-    r_hi = min(r_hi, r_lo + per);
+    const int per = (rows + p.splits - 1) / p.splits;
+    r_lo = min(rows, (int)blockIdx.y * per);
+    r_hi = min(rows, r_lo + per);
   }
 }
 
@@ -549,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         tma_load_2d_hint(stage_w(kb), &tmW, (kb0 + kb) * kBK, n0, &full[kb], pol);
       }
       pdl_wait();
-      pdl_launch_dependents();
+      if (!p.late_dependents) pdl_launch_dependents();
       for (int kb = 0; kb < pre; ++kb) tma_load_2d(stage_x(kb), &tmX, (kb0 + kb) * kBK, m0, &full[kb]);
       for (int kb = pre; kb < nkb; ++kb) {
         const int s = kb % C::kStages;
@@ -573,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   // -------------------------------------------------------------- consumers
   pdl_wait();
-  pdl_launch_dependents();
+  if (!p.late_dependents) pdl_launch_dependents();
   const int tid = threadIdx.x;  // 0..255
   EpiPre<EPI, kConsumers, BM> pre;
   epi_prefetch<EPI, kConsumers, BM>(p, pre, m0, n0, tid, warp, lane);
@@ -650,6 +652,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   named_sync<kConsumers>();
   finish_tile<EPI, kConsumers, BM>(p, pre, tile, s_scale, m0, n0, tid, warp, lane);
+  if (p.late_dependents) pdl_launch_dependents();
   if (p.splits > 1) cluster_wait();  // the other splits are done reading this CTA's tile
 }
 
@@ -772,7 +775,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         tma_load_2d_hint(stage_w(kb), &tmW, (kb0 + kb) * kBK, n0, &full[kb], pol);
       }
       pdl_wait();
-      pdl_launch_dependents();
+      if (!p.late_dependents) pdl_launch_dependents();
       for (int kb = 0; kb < pre; ++kb) tma_load_2d(stage_x(kb), &tmX, (kb0 + kb) * kBK, m0, &full[kb]);
       for (int kb = pre; kb < nkb; ++kb) {
         const int s = kb % C::kStages;
@@ -813,7 +816,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   } else {
     // ----------------------------------- TMEM -> tile / partials (warps 2..5)
     pdl_wait();
-    pdl_launch_dependents();
+    if (!p.late_dependents) pdl_launch_dependents();
     const int q = warp & 3;            // TMEM lane quarter this warp may access
     const int nl = q * 32 + lane;      // weight row of this thread within the tile
     tc_prep<EPI, NT>(p, m0, n0, s_scale, s_rs, s_ps, threadIdx.x - 64, warp - 2, lane);
@@ -852,6 +855,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   EpiPre<EPI, kTcThreads, NT> pre;  // loads its epilogue inputs row by row
   finish_tile<EPI, kTcThreads, NT, true, 8>(p, pre, reinterpret_cast<float*>(smem), s_scale, m0, n0, threadIdx.x,
                                             warp, lane, s_rs, s_ps);
+  if (p.late_dependents) pdl_launch_dependents();
   if (p.splits > 1) cluster_wait();  // the other splits are done reading this CTA's tile
 }
 
@@ -883,12 +887,16 @@ cudaError_t configure() {
 
 // Split-K runs each tile's splits as one cluster of (1, splits, 1) CTAs.
 template <int BM, int EPI>
-cudaError_t launch_proj(const CUtensorMap* tmW, const CUtensorMap* tmX, const EpiParams& p, cudaStream_t st) {
+cudaError_t launch_proj(const CUtensorMap* tmW, const CUtensorMap* tmX, EpiParams p, cudaStream_t st) {
   using K = Kern<BM, EPI>;
   if (cudaError_t e = configure<BM, EPI>()) return e;
   // token tiles fastest: the tiles of one weight slab are dispatched side by side,
   // so a slab streamed from HBM for one token tile is still in L2 for the next
   dim3 grid((p.M + BM - 1) / BM, p.splits, p.N / kBN);
+  // two CTAs per SM: a grid beyond that is more than one wave (measured at 320 rows:
+  // the gate/up projection's 672 CTAs releasing the down projection early left part
+  // of down's clusters for a second wave, +25 us per layer)
+  p.late_dependents = (long long)grid.x * grid.y * grid.z > 2LL * p.sm_count ? 1 : 0;
   if (p.splits == 1) return launch_k(K::fn(), grid, dim3(K::kThreadsPerCta), K::kSmem, st, *tmW, *tmX, p);
   return launch_k_cluster(K::fn(), grid, dim3(K::kThreadsPerCta), K::kSmem, st, dim3(1, p.splits, 1), *tmW, *tmX,
                           p);

@@ -59,6 +59,12 @@ struct EpiParams {
   // kernel starts); split evenly over the CTAs.  Null / 0: none.
   const void* l2_next;
   unsigned long long l2_next_bytes;  // multiple of 16
+  int sm_count;
+  // Set by the launcher: release the next kernel (programmatic dependent launch) only
+  // as each CTA finishes, for grids of more than one wave.  Released early, the next
+  // grid's clusters are placed piecemeal on the slots this grid's last wave frees and
+  // part of it ends up in a second wave.
+  int late_dependents;
   int* status;
 };
 cudaError_t launch_gemm_epi(int epi, const CUtensorMap* tmW, const CUtensorMap* tmX, int BM, EpiParams p,
