@@ -432,9 +432,11 @@ def test_long_context_attention_matches_oracle():
         m.close()
 
 
-def test_many_sequences_single_cta_attention():
+@pytest.mark.parametrize("W", [3, 4])
+def test_many_sequences_single_cta_attention(W):
     """40 sequences x 4 kv heads leave one CTA per (sequence, kv head) in one wave
-    (no cluster merge): logits and the written KV still match the oracle."""
+    (no cluster merge): logits and the written KV still match the oracle.  At width
+    4 the 160 rows take two tcgen05 token tiles (128 + a ragged 32)."""
     need_gpu()
     w = synth.make_weights(synth.TINY, seed=9, gain_jitter=0.1)
     B = 40
@@ -452,7 +454,7 @@ def test_many_sequences_single_cta_attention():
         m.prefill(ids, tok.cuda(), lens.tolist())
         o = oracle_for(synth.TINY, w, **kw)
         o.prefill(ids, prompts)
-        win = np.concatenate([np.array([[pr[-1]] for pr in prompts]), g.integers(0, synth.TINY.vocab, (B, 2))], 1)
+        win = np.concatenate([np.array([[pr[-1]] for pr in prompts]), g.integers(0, synth.TINY.vocab, (B, W - 1))], 1)
         got = m.score(ids, torch.from_numpy(win).cuda()).cpu().numpy()
         assert rel_err(got, o.forward(ids, win)) < TOL
         lens_m, pt = m.kv_state(ids)
