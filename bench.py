@@ -633,20 +633,23 @@ class OracleSample:
         p = A.target_probs(logits, a.temperature)
         n, com, bonus, _ = A.accept_stochastic(p, q, tok[:, 1:], u)
         t1 = _t.perf_counter()
-        _ = hid @ o.w("lm_head").T
-        t2 = _t.perf_counter()
+        if a.cpu_layers < a.layers:      # a sample of the layers: time the LM head alone, scale the rest
+            _ = hid @ o.w("lm_head").T
+            head = _t.perf_counter() - t1
+            full = max(t1 - t0 - head, 0.0) / a.cpu_layers * a.layers + head
+        else:                            # the whole model: the measured time as it is
+            full = t1 - t0
         o.commit([0], n, W)
         self.pending = int(bonus[0])
         self.r += 1
-        head = t2 - t1
-        full = max(t1 - t0 - head, 0.0) / a.cpu_layers * 32 + head
         return full, int(n[0]) + 1, t1 - t0
 
     def describe(self):
         a = self.args
+        scaled = f"; per-layer time x {a.layers} layers" if a.cpu_layers < a.layers else "; no scaling"
         return (f"verify rounds of width {self.W} at B=1 over {a.cpu_layers} decoder layers of the 8B shape "
                 f"+ LM head + acceptance, {a.ctx} cached tokens of synthetic KV, drafts from the oracle's own p "
-                f"(lam={a.lam}); per-layer time x 32 layers")
+                f"(lam={a.lam}), numpy float64 on the host cores{scaled}")
 
 
 def oracle_tiny_rounds_per_s(n_rounds=8):
@@ -698,11 +701,24 @@ def cpu_threads():
     return os.cpu_count()
 
 
+def workload_config(args, world):
+    """The `config` object of a bench line (both arms: the same workload)."""
+    return {"workload": f"llama3.1-8b-shape ({args.layers} layers) sampled verify round, "
+                        f"B={args.batch}/GPU, ctx={args.ctx}, gamma={args.gamma} (width {args.gamma + 1}), "
+                        f"lam={args.lam}, T={args.temperature}",
+            "global_batch": args.batch * world, "seq_len": args.ctx, "gamma": args.gamma, "lam": args.lam,
+            "l2": "no flush: every step streams 15 GB of weights (inputs larger than L2)",
+            "parallelism": f"replicas x{world}"}
+
+
 def run_reference(args):
-    """The oracle as it stands on the host cores: W untimed + K timed sample rounds."""
+    """The oracle as it stands on the host cores: W untimed + K timed rounds over all
+    of the model's layers (no projection from a sample: ~1 s per width-5 round, ~80 GB
+    of float64 weights on the host)."""
     rank, _, world = dist_env()
     if rank != 0:
         return
+    args.cpu_layers = args.layers
     smp = OracleSample(args)
     for _ in range(min(args.warmup, 1)):
         smp.step()
@@ -715,9 +731,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1000 * secs / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": f"llama3.1-8b-shape sampled verify round, B={args.batch}/GPU, ctx={args.ctx}, "
-                                   f"gamma={args.gamma} (width {args.gamma + 1}), lam={args.lam}, "
-                                   f"T={args.temperature}"},
+            "config": workload_config(args, 1),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
                              "sample": smp.describe()},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -805,12 +819,7 @@ def main():
            "scaling": "weak", "vs_baseline": None, "dtype": "f16",
            "data": "synthetic: random-init N(0,0.02) bf16 weights, random-token prompts, drafts from "
                    "q=(1-lam)p+lam*Dir(1) with p the target at the draft prefix",
-           "config": {"workload": f"llama3.1-8b-shape ({args.layers} layers) sampled verify round, "
-                                  f"B={args.batch}/GPU, ctx={args.ctx}, gamma={gamma} (width {gamma + 1}), "
-                                  f"lam={lam}, T={temp}",
-                      "global_batch": args.batch * world, "seq_len": args.ctx, "gamma": gamma, "lam": lam,
-                      "l2": "no flush: every step streams 15 GB of weights (inputs larger than L2)",
-                      "parallelism": f"replicas x{world}"},
+           "config": workload_config(args, world),
            "gpu_launches": launches * args.steps, "replay_matches_record": replay_ok,
            "accept": {"tokens_per_round": round(mean_tpr, 4), "strict_accept_rate": round(strict, 4),
                       "accept_length": round(mean_tpr, 4), "width_proxy": round(mean_tpr / (gamma + 1), 4)},
