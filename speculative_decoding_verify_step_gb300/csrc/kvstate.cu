@@ -126,9 +126,13 @@ __global__ void __launch_bounds__(32) alloc_to_len_kernel(const int32_t* seq_ids
       continue;
     }
     const int upto = relative ? seq_len[s] + lens[i] : lens[i];
+    const int npg0 = seq_npages[s];
     const bool ok = warp_ensure_pages(s, upto, seq_npages, page_table, max_pages, free_bits, num_pages);
     if (threadIdx.x == 0) {
-      if (!ok) set_status(status, SPEC_ERR_CAPACITY);
+      if (!ok) {  // give back what this call took: the sequence keeps the pages it had
+        set_status(status, SPEC_ERR_CAPACITY);
+        release_pages_from(s, npg0, seq_npages, page_table, max_pages, free_bits);
+      }
       if (!relative) seq_len[s] = ok ? lens[i] : 0;
     }
     __syncwarp();

@@ -406,6 +406,44 @@ def test_verify_round_on_an_exhausted_pool_keeps_the_length(tiny):
         m.close()
 
 
+def test_kv_write_gives_a_sequence_the_callers_cache(tiny):
+    """spec_kv_write: the values read back bit for bit, pages taken lowest first, the
+    length set; an exhausted pool reports SPEC_ERR_CAPACITY; wrong shapes are refused."""
+    need_gpu()
+    from speculative_decoding_verify_step_gb300 import spec
+    w, _ = tiny
+    dims = synth.TINY
+    m = cuda_model(dims, w, max_batch=2, max_width=4, max_seq_len=256, num_pages=5)
+    try:
+        m.seq_reset([0, 1])
+        shape = (dims.n_layers, 130, dims.n_kv_heads, dims.head_dim)
+        k = synth.normal_fill(shape, seed=1, std=1.0, dtype=torch.float16)
+        v = synth.normal_fill(shape, seed=2, std=1.0, dtype=torch.float16)
+        m.kv_write(1, k, v)
+        m.sync_status()
+        lens, pt = m.kv_state([1])
+        assert lens == [130] and pt[0][:3] == [0, 1, 2] and pt[0][3] == -1
+        for layer in range(dims.n_layers):
+            kr, vr = m.read_kv(layer, 1, 0, 130)
+            assert torch.equal(kr, k[layer]) and torch.equal(vr, v[layer])
+        m.kv_write(0, k[:, :100], v[:, :100])      # needs 2 pages, 2 left
+        m.sync_status()
+        assert m.kv_state([0])[1][0][:2] == [3, 4]
+        m.kv_write(0, k[:, :129], v[:, :129])      # 3 pages: one short after its own 2 return
+        with pytest.raises(spec.SpecError) as e:
+            m.sync_status()
+        assert e.value.status == 4
+        lens, pt = m.kv_state([0])
+        assert lens == [0] and pt[0][0] == -1           # the pages it took went back to the pool
+        m.kv_write(0, k[:, :100], v[:, :100])
+        m.sync_status()
+        assert m.kv_state([0])[1][0][:2] == [3, 4]
+        with pytest.raises(ValueError):
+            m.kv_write(0, k[:1], v[:1])            # wrong layer count
+    finally:
+        m.close()
+
+
 def test_long_context_attention_matches_oracle():
     """A 4200-token cache: 66 pages per sequence, 5 per CTA of the 16-CTA cluster,
     so the attention splits each page's keys over four warps and combines their
