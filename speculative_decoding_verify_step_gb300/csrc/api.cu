@@ -75,6 +75,7 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+constexpr int kPairBoxes = 16;
 constexpr int kNumBM = 4;
 constexpr int kBMs[kNumBM] = {8, 16, 64, 128};
 int bm_index(int bm) {
@@ -128,6 +129,9 @@ struct spec_model {
   int32_t *scratch_ids = nullptr, *scratch_ids2 = nullptr, *scratch_tok = nullptr, *scratch_lens = nullptr;
   int32_t *scratch_acc = nullptr, *scratch_bonus = nullptr;
   CUtensorMap tm_xn[kNumBM], tm_attn[kNumBM], tm_act[kNumBM];
+  // CTA-pair kernel: boxes of 8, 16, .., 128 token rows (half a token tile)
+  CUtensorMap tm_xn2[kPairBoxes], tm_attn2[kPairBoxes], tm_act2[kPairBoxes];
+  bool pair_ok = false;  // every projection's N is a multiple of 256 (the pair's weight rows)
   int M_alloc = 0;  // rows of the activation buffers (>= 256 for the widest token tile)
   int last_rows = 0, last_launches = 0;
   // profiling: event pairs around projection / attention launches
@@ -238,8 +242,13 @@ spec_status forward(spec_model* m, int B, int W, const int32_t* seq_ids, const i
   CUDA_TRY(launch_embed(tok, M, m->embed, m->layers[0].attn_norm, d, c.vocab, m->resid, m->xn, m->ssq_a, m->M_max,
                         m->status, st));
 
-  const int BM = choose_bm(M);
+  const bool pair = m->pair_ok && pair_rows(M);
+  const int BM = pair ? kPairBM : choose_bm(M);
   const int bi = bm_index(BM);
+  const int pbox = pair ? pair_tile_rows(M) / 16 - 1 : 0;
+  const CUtensorMap* tmx_xn = pair ? &m->tm_xn2[pbox] : &m->tm_xn[bi];
+  const CUtensorMap* tmx_attn = pair ? &m->tm_attn2[pbox] : &m->tm_attn[bi];
+  const CUtensorMap* tmx_act = pair ? &m->tm_act2[pbox] : &m->tm_act[bi];
   auto splits_for = [&](int N, int K) {
     return choose_splits(N, K, M, BM, m->sm_count, 16);
   };
@@ -311,7 +320,7 @@ spec_status forward(spec_model* m, int B, int W, const int32_t* seq_ids, const i
       e.q_out = m->qrot;
       e.kpool = m->kpool + l * layer_elems;
       e.vpool = m->vpool + l * layer_elems;
-      CUDA_TRY(profiled(m, 0, wb_qkv, st, [&] { return launch_gemm_epi(kEpiQKV, &Ly.tm_qkv, &m->tm_xn[bi], BM, e, st); }));
+      CUDA_TRY(profiled(m, 0, wb_qkv, st, [&] { return launch_gemm_epi(kEpiQKV, &Ly.tm_qkv, tmx_xn, BM, e, st); }));
     }
     ap.layer_row0 = l * c.num_pages * Hkv * kPage;
     CUDA_TRY(profiled(m, 5, kv_bytes, st, [&] { return launch_attention(&m->tm_k, &m->tm_v, ap, st); }));
@@ -329,7 +338,7 @@ spec_status forward(spec_model* m, int B, int W, const int32_t* seq_ids, const i
       e.d = d;
       e.l2_next = reinterpret_cast<const char*>(Ly.wgu) + pf_gu;
       e.l2_next_bytes = (unsigned long long)std::min(proj_pf, wb_gu - (double)pf_gu) & ~15ull;
-      CUDA_TRY(profiled(m, 1, wb_o, st, [&] { return launch_gemm_epi(kEpiResid, &Ly.tm_o, &m->tm_attn[bi], BM, e, st); }));
+      CUDA_TRY(profiled(m, 1, wb_o, st, [&] { return launch_gemm_epi(kEpiResid, &Ly.tm_o, tmx_attn, BM, e, st); }));
     }
     {
       EpiParams e = base;
@@ -342,7 +351,7 @@ spec_status forward(spec_model* m, int B, int W, const int32_t* seq_ids, const i
       e.ffn = F;
       e.l2_next = Ly.wdown;
       e.l2_next_bytes = (unsigned long long)std::min(proj_pf, wb_dn) & ~15ull;
-      CUDA_TRY(profiled(m, 2, wb_gu, st, [&] { return launch_gemm_epi(kEpiSwiGLU, &Ly.tm_gu, &m->tm_xn[bi], BM, e, st); }));
+      CUDA_TRY(profiled(m, 2, wb_gu, st, [&] { return launch_gemm_epi(kEpiSwiGLU, &Ly.tm_gu, tmx_xn, BM, e, st); }));
     }
     {
       EpiParams e = base;
@@ -363,7 +372,7 @@ spec_status forward(spec_model* m, int B, int W, const int32_t* seq_ids, const i
         e.l2_next = m->lm_head;
         e.l2_next_bytes = (unsigned long long)std::min(proj_pf, 2.0 * c.vocab * d) & ~15ull;
       }
-      CUDA_TRY(profiled(m, 3, wb_dn, st, [&] { return launch_gemm_epi(kEpiResid, &Ly.tm_down, &m->tm_act[bi], BM, e, st); }));
+      CUDA_TRY(profiled(m, 3, wb_dn, st, [&] { return launch_gemm_epi(kEpiResid, &Ly.tm_down, tmx_act, BM, e, st); }));
     }
   }
   if (want_logits) {
@@ -379,7 +388,7 @@ spec_status forward(spec_model* m, int B, int W, const int32_t* seq_ids, const i
     e.tstat_sum = sampled ? m->tstat_sum : nullptr;
     e.tstat_arg = m->tstat_arg;
     e.tstat_stride = m->M_max;
-    CUDA_TRY(profiled(m, 4, 2.0 * c.vocab * d, st, [&] { return launch_gemm_epi(kEpiLogits, &m->tm_lm, &m->tm_xn[bi], BM, e, st); }));
+    CUDA_TRY(profiled(m, 4, 2.0 * c.vocab * d, st, [&] { return launch_gemm_epi(kEpiLogits, &m->tm_lm, tmx_xn, BM, e, st); }));
     m->last_rows = M;
   }
   return SPEC_OK;
@@ -650,6 +659,12 @@ spec_status spec_model_create(const spec_config* cfg, spec_model** out) {
     ok &= make_map(&m->tm_act[i], m->act, F, m->M_alloc, 64, kBMs[i]);
   }
   const uint64_t kv_rows = (uint64_t)c.n_layers * c.num_pages * c.n_kv_heads * kPage;
+  for (int i = 0; i < kPairBoxes; ++i) {
+    ok &= make_map(&m->tm_xn2[i], m->xn, d, m->M_alloc, 64, 8 * (i + 1));
+    ok &= make_map(&m->tm_attn2[i], m->attn_out, m->q_dim, m->M_alloc, 64, 8 * (i + 1));
+    ok &= make_map(&m->tm_act2[i], m->act, F, m->M_alloc, 64, 8 * (i + 1));
+  }
+  m->pair_ok = m->qkv_n % 256 == 0 && d % 256 == 0 && (2 * F) % 256 == 0 && V % 256 == 0;
   ok &= make_map(&m->tm_k, m->kpool, hd, kv_rows, 64, 64);
   ok &= make_map(&m->tm_v, m->vpool, hd, kv_rows, 64, 64);
   if (!ok) return bail(fail(SPEC_ERR_CUDA, "tensor map encoding failed"));

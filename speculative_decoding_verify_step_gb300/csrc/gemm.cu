@@ -65,12 +65,13 @@ SPEC_DEVICE_INLINE void named_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(N) : "memory");
 }
 
-// Rows [r_lo, r_hi) of the token tile that this CTA finishes: all of them, or with
-// split-K the share of split blockIdx.y of the tile's real rows (a ragged tile of 80
+// Rows [r_lo, r_hi) of the token tile (at most `cap` rows from m0) that this CTA
+// finishes: all of them, or with split-K the share of split blockIdx.y of the
+// tile's real rows (a ragged tile of 80
 // rows over 8 splits: 10 rows each, not 16 rows for five of them).
 template <int ROWS>
-SPEC_DEVICE_INLINE void tile_rows(const EpiParams& p, int m0, int& r_lo, int& r_hi) {
-  const int rows = min(ROWS, p.M - m0);
+SPEC_DEVICE_INLINE void tile_rows(const EpiParams& p, int m0, int& r_lo, int& r_hi, int cap = ROWS) {
+  const int rows = max(0, min(cap, p.M - m0));
   r_lo = 0;
   r_hi = rows;
   if (p.splits > 1) {
@@ -152,7 +153,7 @@ SPEC_DEVICE_INLINE void epi_prefetch(const EpiParams& p, EpiPre<EPI, NT, ROWS>& 
 // order on every run).  U items per thread are in flight at a time, their S
 // remote loads each issued before any is used.
 template <int S, int U, int NT>
-SPEC_DEVICE_INLINE void reduce_rows(float* tile, int r_lo, int n_items, int tid) {
+SPEC_DEVICE_INLINE void reduce_rows(float* tile, int r_lo, int n_items, int tid, int rank0, int rstep) {
   for (int e0 = tid; e0 < n_items; e0 += U * NT) {
     float4 a[U][S];
 #pragma unroll
@@ -160,7 +161,7 @@ SPEC_DEVICE_INLINE void reduce_rows(float* tile, int r_lo, int n_items, int tid)
       const int e = min(e0 + u * NT, n_items - 1);
       const uint32_t off = smem_u32(tile + (r_lo + e / (kBN / 4)) * kTilePad + (e % (kBN / 4)) * 4);
 #pragma unroll
-      for (int j = 0; j < S; ++j) a[u][j] = ld_dsmem_f4(mapa_u32(off, j));
+      for (int j = 0; j < S; ++j) a[u][j] = ld_dsmem_f4(mapa_u32(off, rank0 + j * rstep));
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -180,7 +181,8 @@ SPEC_DEVICE_INLINE void reduce_rows(float* tile, int r_lo, int n_items, int tid)
 }
 
 template <int NT, int LOADS, int S = 2>
-SPEC_DEVICE_INLINE void reduce_splits(int splits, float* tile, int r_lo, int n_items, int tid) {
+SPEC_DEVICE_INLINE void reduce_splits(int splits, float* tile, int r_lo, int n_items, int tid, int rank0 = 0,
+                                      int rstep = 1) {
   if constexpr (LOADS == 1) {
     // one item at a time: a single loop for every split count (measured: the
     // specialised copies cost more in instruction fetch than they save here)
@@ -190,7 +192,7 @@ SPEC_DEVICE_INLINE void reduce_splits(int splits, float* tile, int r_lo, int n_i
       float4 a[kMaxSplits];
 #pragma unroll
       for (int j = 0; j < kMaxSplits; ++j)
-        if (j < splits) a[j] = ld_dsmem_f4(mapa_u32(off, j));
+        if (j < splits) a[j] = ld_dsmem_f4(mapa_u32(off, rank0 + j * rstep));
       float4 v = a[0];
 #pragma unroll
       for (int j = 1; j < kMaxSplits; ++j)
@@ -204,9 +206,9 @@ SPEC_DEVICE_INLINE void reduce_splits(int splits, float* tile, int r_lo, int n_i
     }
   } else if constexpr (S <= kMaxSplits) {
     if (splits == S) {
-      reduce_rows<S, (LOADS / S > 1 ? LOADS / S : 1), NT>(tile, r_lo, n_items, tid);
+      reduce_rows<S, (LOADS / S > 1 ? LOADS / S : 1), NT>(tile, r_lo, n_items, tid, rank0, rstep);
     } else {
-      reduce_splits<NT, LOADS, S + 1>(splits, tile, r_lo, n_items, tid);
+      reduce_splits<NT, LOADS, S + 1>(splits, tile, r_lo, n_items, tid, rank0, rstep);
     }
   }
 }
@@ -217,8 +219,10 @@ SPEC_DEVICE_INLINE void reduce_splits(int splits, float* tile, int r_lo, int n_i
 // thread-block cluster: after a cluster barrier, split r sums rows
 // [r * ROWS/S, (r+1) * ROWS/S) of all S partial tiles through distributed shared
 // memory, in split order (deterministic), and runs the epilogue on those rows --
-// the reduction is spread over the S CTAs and never leaves the chip.  The caller
-// holds back the CTA's exit with the matching cluster_wait().
+// the reduction is spread over the S CTAs and never leaves the chip.  Split j's
+// partial tile sits in the CTA of cluster rank rank0 + j * rstep (the CTA pairs of
+// the pair kernel interleave their splits).  The caller holds back the CTA's exit
+// with the matching cluster_wait().
 //
 // PREP: the weight-row scales, the row scales and (QKV) the rows' positions and
 // KV slots were already placed in s_rs / s_scale / s_ps while the mainloop ran;
@@ -226,15 +230,17 @@ SPEC_DEVICE_INLINE void reduce_splits(int splits, float* tile, int r_lo, int n_i
 template <int EPI, int NT, int ROWS, bool PREP = false, int LOADS = 1>
 SPEC_DEVICE_INLINE void finish_tile(const EpiParams& p, const EpiPre<EPI, NT, ROWS>& pre, float* tile,
                                     float* s_scale, int m0, int n0, int tid, int warp, int lane,
-                                    float* s_rs_prep = nullptr, const int2* s_ps = nullptr) {
+                                    float* s_rs_prep = nullptr, const int2* s_ps = nullptr, int rank0 = 0,
+                                    int rstep = 1, int rows_cap = ROWS) {
   using E = EpiPre<EPI, NT, ROWS>;
   constexpr int kGroupWarps = NT / 32;
   int r_lo, r_hi;
-  tile_rows<ROWS>(p, m0, r_lo, r_hi);
+  tile_rows<ROWS>(p, m0, r_lo, r_hi, rows_cap);
   if (p.splits > 1) {
     cluster_arrive();  // this CTA's partial tile is written
     cluster_wait();    // ... and every other split's
-    reduce_splits<NT, LOADS>(p.splits, tile, r_lo, max(0, r_hi - r_lo) * (kBN / 4), tid);
+    reduce_splits<NT, LOADS>(p.splits, tile, r_lo, max(0, r_hi - r_lo) * (kBN / 4), tid, rank0, rstep);
+    __syncwarp();      // converged for the aligned cluster barrier
     cluster_arrive();  // done reading the other CTAs' tiles
   }
   // weight-row scale 2^-e of the fp16 encoding, per output column of the tile
@@ -653,6 +659,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   named_sync<kConsumers>();
   finish_tile<EPI, kConsumers, BM>(p, pre, tile, s_scale, m0, n0, tid, warp, lane);
   if (p.late_dependents) pdl_launch_dependents();
+  __syncwarp();
   if (p.splits > 1) cluster_wait();  // the other splits are done reading this CTA's tile
 }
 
@@ -689,11 +696,9 @@ struct TcCfg {
 // of the tile's columns, the row scale of each row this split finishes (sum of
 // the previous kernel's per-tile r^2, in the same order as the epilogue would)
 // and, for QKV, each row's position and KV slot.
-template <int EPI, int NT>
+template <int EPI>
 SPEC_DEVICE_INLINE void tc_prep(const EpiParams& p, int m0, int n0, float* s_scale, float* s_rs, int2* s_ps, int t,
-                                int w, int lane) {
-  int r_lo, r_hi;
-  tile_rows<NT>(p, m0, r_lo, r_hi);
+                                int w, int lane, int r_lo, int r_hi) {
   s_rs[t] = __ldg(p.rscale + n0 + t);
   for (int r0 = r_lo + w; r0 < r_hi; r0 += 8 * 4) {  // eight rows per warp at a time
     float ss[8];
@@ -819,7 +824,9 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     if (!p.late_dependents) pdl_launch_dependents();
     const int q = warp & 3;            // TMEM lane quarter this warp may access
     const int nl = q * 32 + lane;      // weight row of this thread within the tile
-    tc_prep<EPI, NT>(p, m0, n0, s_scale, s_rs, s_ps, threadIdx.x - 64, warp - 2, lane);
+    int r_lo, r_hi;
+    tile_rows<NT>(p, m0, r_lo, r_hi);
+    tc_prep<EPI>(p, m0, n0, s_scale, s_rs, s_ps, threadIdx.x - 64, warp - 2, lane, r_lo, r_hi);
     const bool done = mbar_wait(accum, 0, p.status);
     tc_fence_after();
     if (!done) s_fail = 1;
@@ -856,7 +863,246 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   finish_tile<EPI, kTcThreads, NT, true, 8>(p, pre, reinterpret_cast<float*>(smem), s_scale, m0, n0, threadIdx.x,
                                             warp, lane, s_rs, s_ps);
   if (p.late_dependents) pdl_launch_dependents();
+  __syncwarp();
   if (p.splits > 1) cluster_wait();  // the other splits are done reading this CTA's tile
+}
+
+// ----------------------------------------------------------------------------
+// CTA-pair path (tcgen05 cta_group::2) from 65 token rows: two CTAs on two SMs
+// share one MMA of 256 weight rows x N token rows (N up to 256).  Each CTA stages
+// its own 128 weight rows and half of the tile's token rows per k-block (the pair
+// MMA reads A and B from both CTAs' shared memory) and receives 128 lanes x N
+// columns of the accumulator in its own tensor memory.  Per SM that is half the
+// staged bytes per MMA of a single-CTA tile with the same token rows, and one
+// weight slab serves up to 256 token rows (one pass over the weights up to 256
+// rows, where 128-row single-CTA tiles read each slab twice).
+//   * Warp 0 of each CTA drives TMA into its own stages; the loads complete on
+//     the even CTA's barrier, which expects both CTAs' bytes.
+//   * One thread of the even CTA issues the pair MMAs and commits each stage to
+//     the empty barriers of both CTAs (multicast), and the accumulator likewise.
+//   * Warps 2..5 of each CTA stage the epilogue inputs, then read their CTA's
+//     accumulator out of tensor memory in chunks of at most 192 token rows and,
+//     with the other two warps, run the common tile finish on each chunk (the
+//     fp32 chunk, rows x 132 x 4 bytes, reuses the pipeline buffers).
+// Split-K runs as a cluster of (2, S, 1) CTAs: the pair of split j holds cluster
+// ranks 2j and 2j + 1.  Two CTAs per SM.
+// Tensor memory: a pair allocates the same columns on both of its SMs.  With the
+// pair on the two SMs of one TPC, both SMs hold the same CTAs' allocations, so a
+// pair never waits for columns that are free on one SM only (a wait that a CTA
+// holding columns on the other SM, itself waiting at a cluster barrier for this
+// pair, could never end).  Each pair checks its placement before it allocates
+// and, placed otherwise, computes nothing and reports SPEC_ERR_UNSUPPORTED.
+constexpr int kTc2PipeBytes = 104 * 1024;
+constexpr int kTc2MaxRows = 256;    // token rows per tile (MMA N)
+constexpr int kTc2ChunkRows = 192;  // token rows per epilogue chunk
+constexpr int kTc2MaxStages = 8;
+static_assert(kTc2ChunkRows * kTilePad * 4 <= kTc2PipeBytes, "epilogue chunk reuses the pipeline buffers");
+
+struct Tc2Cfg {
+  // barriers, TMEM address, row scales [rows], weight-row scales [kBN], (position, slot) [rows]
+  static constexpr int kSmemBytes =
+      kTc2PipeBytes + (2 * kTc2MaxStages + 1) * 8 + 16 + 16 + kTc2MaxRows * 4 + kBN * 4 + kTc2MaxRows * 8 + 1024;
+};
+// two CTAs per SM (228 KB of shared memory per SM, 1 KB reserved per CTA), and no third
+static_assert(2 * (Tc2Cfg::kSmemBytes + 1024) <= 228 * 1024 && 3 * (Tc2Cfg::kSmemBytes + 1024) > 228 * 1024,
+              "the pair kernel runs two CTAs per SM");
+
+template <int EPI>
+__global__ void __launch_bounds__(kTcThreads, 2)
+    gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                    const __grid_constant__ EpiParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kTc2PipeBytes);
+  uint64_t* empty = full + kTc2MaxStages;
+  uint64_t* accum = empty + kTc2MaxStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
+  float* s_scale = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(tmem_slot + 4) + 15) & ~uintptr_t(15));
+  float* s_rs = s_scale + kTc2MaxRows;
+  int2* s_ps = reinterpret_cast<int2*>(s_rs + kBN);
+  __shared__ int s_fail;
+  __shared__ uint32_t s_sm;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int pr = blockIdx.x & 1;               // position in the pair: 0 issues the MMAs
+  const uint32_t crank = cluster_ctarank();    // pr + 2 * blockIdx.y
+  const uint32_t lead = crank & ~1u;
+  const int n0 = blockIdx.z * (2 * kBN) + pr * kBN;
+  const int m0 = (blockIdx.x >> 1) * p.tok_tile;
+  const int rows = min(p.tok_tile, p.M - m0);
+  const int n_act = min(p.tok_tile, (rows + 15) & ~15);  // MMA N: the tile's rows rounded up to 16
+  const int xbox = p.tok_tile / 2;                      // token rows per CTA and stage (TMA box)
+  const int stage_bytes = kBN * kBK * 2 + xbox * kBK * 2;
+  const int stages = min(kTc2MaxStages, kTc2PipeBytes / stage_bytes);
+  const uint32_t tmem_cols = n_act <= 32 ? 32 : n_act <= 64 ? 64 : n_act <= 128 ? 128 : 256;
+  const int ch = p.tok_chunk;                          // epilogue chunk rows (same for every tile)
+  const int nch = (p.tok_tile + ch - 1) / ch;
+  const int kb0 = blockIdx.y * p.kb_per_split;
+  const int nkb = min(p.kb_per_split, p.kb_total - kb0);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(accum, 1);
+    s_fail = 0;
+    s_sm = sm_id();
+    fence_barrier_init();
+  }
+  __syncwarp();
+  // The peer's loads complete on the even CTA's barriers and the even CTA's MMAs
+  // commit to both CTAs' barriers: all of them are initialised before either runs.
+  cluster_arrive();
+  cluster_wait();
+  // the pair on the two SMs of one TPC (SM ids 2t, 2t + 1), or nothing at all
+  const bool placed = (ld_dsmem_u32(mapa_u32(smem_u32(&s_sm), crank ^ 1u)) ^ sm_id()) == 1u;
+  if (!placed && threadIdx.x == 0) {
+    s_fail = 1;
+    if (pr == 0) set_status(p.status, SPEC_ERR_UNSUPPORTED);
+  }
+  const int pre = min(nkb, stages);
+  const uint64_t pol = l2_policy_evict_first();
+  if (placed && threadIdx.x == 0 && nkb > 0) {  // weights never depend on the previous kernel
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmX);
+    for (int kb = 0; kb < pre; ++kb) {
+      if (pr == 0) mbar_arrive_expect_tx(&full[kb], 2 * stage_bytes);
+      tma_load_2d_pair_hint(smem + kb * stage_bytes, &tmW, (kb0 + kb) * kBK, n0,
+                            mapa_u32(smem_u32(&full[kb]), lead), pol);
+    }
+  }
+  __syncwarp();
+  if (warp == 1 && placed) {
+    tmem_alloc2(tmem_slot, tmem_cols);
+    tmem_relinquish2();
+  }
+  tc_fence_before();
+  cluster_arrive();  // both CTAs of every pair hold their tensor memory
+  cluster_wait();
+  tc_fence_after();
+  const uint32_t tmem = placed ? *tmem_slot : 0u;
+
+  auto stage_w = [&](int s) { return smem + s * stage_bytes; };
+  auto stage_x = [&](int s) { return smem + s * stage_bytes + kBN * kBK * 2; };
+
+  if (!placed) {
+    // nothing staged, nothing issued: straight to the failure path below
+  } else if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && nkb > 0) {
+      const int xrow = m0 + pr * (n_act / 2);  // this CTA's half of the MMA's token rows
+      pdl_wait();
+      if (!p.late_dependents) pdl_launch_dependents();
+      for (int kb = 0; kb < pre; ++kb)
+        tma_load_2d_pair(stage_x(kb), &tmX, (kb0 + kb) * kBK, xrow, mapa_u32(smem_u32(&full[kb]), lead));
+      for (int kb = pre; kb < nkb; ++kb) {
+        const int s = kb % stages;
+        const uint32_t use = kb / stages;
+        if (!mbar_wait(&empty[s], (use - 1) & 1, p.status)) break;
+        const uint32_t bar = mapa_u32(smem_u32(&full[s]), lead);
+        if (pr == 0) mbar_arrive_expect_tx(&full[s], 2 * stage_bytes);
+        tma_load_2d_pair_hint(stage_w(s), &tmW, (kb0 + kb) * kBK, n0, bar, pol);
+        tma_load_2d_pair(stage_x(s), &tmX, (kb0 + kb) * kBK, xrow, bar);
+      }
+      l2_prefetch_share(p.l2_next, p.l2_next_bytes);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------------------------------- pair MMA issue (even CTA, 1 thread)
+    if (lane == 0 && pr == 0) {
+      const uint32_t idesc = idesc_f16_f32(2 * kBN, n_act);
+      const uint16_t both = (uint16_t)(3u << lead);
+      int kb = 0;
+      for (; kb < nkb; ++kb) {
+        const int s = kb % stages;
+        const uint32_t use = kb / stages;
+        if (!mbar_wait(&full[s], use & 1, p.status)) {
+          s_fail = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t wb = smem_u32(stage_w(s)), xb = smem_u32(stage_x(s));
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk)
+          tc_mma2(tmem, sdesc_k_sw128(wb + kk * 32), sdesc_k_sw128(xb + kk * 32), idesc, (kb | kk) != 0);
+        // the stage is free in both CTAs once these MMAs have read it (committed only
+        // when a producer will wait for it: nothing arrives after the accumulator)
+        if (kb + stages < nkb) tc_commit2_mc(&empty[s], both);
+      }
+      if (nkb <= 0) s_fail = 1;
+      tc_commit2_mc(accum, both);  // arrives in both CTAs when every MMA issued above has completed
+    }
+    __syncwarp();
+  } else {
+    // ------------------- epilogue inputs while the MMAs run (warps 2..5), then wait
+    pdl_wait();
+    if (!p.late_dependents) pdl_launch_dependents();
+    for (int c = 0; c < nch; ++c) {  // the rows this split finishes in each chunk
+      int lo, hi;
+      tile_rows<kTc2ChunkRows>(p, m0 + c * ch, lo, hi, min(ch, p.tok_tile - c * ch));
+      tc_prep<EPI>(p, m0, n0, s_scale, s_rs, s_ps, threadIdx.x - 64, warp - 2, lane, c * ch + lo, c * ch + hi);
+    }
+    const bool done = mbar_wait(accum, 0, p.status);
+    tc_fence_after();
+    if (!done) s_fail = 1;
+  }
+  // A failure seen by either CTA of the pair (a bounded wait that ran out) holds
+  // for both: the flag is copied into the peer before the cluster barrier below.
+  __syncthreads();
+  if (threadIdx.x == 0 && s_fail) st_dsmem_u32(mapa_u32(smem_u32(&s_fail), crank ^ 1u), 1u);
+  __syncwarp();
+  cluster_arrive();
+  cluster_wait();
+  if (s_fail) {
+    for (int c = 0; c < nch; ++c)
+      if (p.splits > 1) {  // still take part in the cluster barriers of each chunk
+        cluster_arrive();
+        cluster_wait();
+        cluster_arrive();
+        cluster_wait();
+      }
+    if (warp == 1 && placed) {
+      tc_fence_after();
+      tmem_dealloc2(tmem, tmem_cols);
+    }
+    return;
+  }
+  if (warp < 2) pdl_wait();  // outputs are written below by every warp
+  float* tile = reinterpret_cast<float*>(smem);  // the pair's MMAs and this CTA's loads are done
+  for (int c = 0; c < nch; ++c) {
+    const int c0 = c * ch;
+    if (warp >= 2) {
+      const int q = warp & 3;        // TMEM lane quarter this warp may access
+      const int nl = q * 32 + lane;  // weight row of this thread within the CTA's 128
+      const int c1 = min(n_act, c0 + ch);
+#pragma unroll 1
+      for (int col = c0; col < c1; col += 16) {
+        float v[16];
+        tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + col, v);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) tile[(col - c0 + i) * kTilePad + nl] = v[i];
+      }
+      tc_fence_before();
+    }
+    __syncthreads();
+    EpiPre<EPI, kTcThreads, kTc2ChunkRows> pre;  // loads its epilogue inputs row by row
+    // rows [c0, c0 + ch) of the token tile, never past its end (or past M)
+    finish_tile<EPI, kTcThreads, kTc2ChunkRows, true, 8>(p, pre, tile, s_scale + c0, m0 + c0, n0, threadIdx.x,
+                                                         warp, lane, s_rs, s_ps + c0, pr, 2,
+                                                         min(ch, p.tok_tile - c0));
+    // The tile is reused by the next chunk once every reader is done: the other
+    // splits (they arrived after reading it) and this CTA's own epilogue threads.
+    __syncwarp();
+    if (p.splits > 1) cluster_wait();
+    __syncthreads();
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc2(tmem, tmem_cols);
+  }
+  if (p.late_dependents) pdl_launch_dependents();
 }
 
 // Kernel, block size and dynamic shared memory of the projection for a token tile.
@@ -902,6 +1148,24 @@ cudaError_t launch_proj(const CUtensorMap* tmW, const CUtensorMap* tmX, EpiParam
                           p);
 }
 
+// Pair kernel: (2 x token tiles, splits, N / 256) CTAs in clusters of (2, splits, 1).
+template <int EPI>
+cudaError_t launch_proj2(const CUtensorMap* tmW, const CUtensorMap* tmX, EpiParams p, cudaStream_t st) {
+  static bool done = false;
+  if (!done) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc2_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Tc2Cfg::kSmemBytes);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(gemm_tc2_kernel<EPI>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    done = true;
+  }
+  const int ntt = (p.M + p.tok_tile - 1) / p.tok_tile;
+  dim3 grid(2 * ntt, p.splits, p.N / (2 * kBN));
+  p.late_dependents = (long long)grid.x * grid.y * grid.z > 2LL * p.sm_count ? 1 : 0;
+  return launch_k_cluster(gemm_tc2_kernel<EPI>, grid, dim3(kTcThreads), Tc2Cfg::kSmemBytes, st,
+                          dim3(2, p.splits, 1), *tmW, *tmX, p);
+}
+
 // How many (1, s, 1) clusters of the projection kernel fit on the GPU at once.
 template <int BM>
 int max_active_clusters(int s) {
@@ -935,6 +1199,7 @@ static_assert(TcCfg<64>::kSmemBytes <= GemmCfg<8>::kSmemBytes && TcCfg<128>::kSm
                   kTcThreads <= kThreads,
               "the mma.sync kernel's footprint bounds the 64/128-row tcgen05 kernel's");
 
+
 int max_active_clusters_bm(int BM, int s) {
   switch (BM) {
     case 8: return max_active_clusters<8>(s);
@@ -951,6 +1216,7 @@ template <int EPI>
 cudaError_t launch_epi(const CUtensorMap* tmW, const CUtensorMap* tmX, int BM, const EpiParams& p,
                        cudaStream_t st) {
   switch (BM) {  // up to 16 token rows: mma.sync (HBM-bound); from 17: tcgen05
+    case kPairBM: return launch_proj2<EPI>(tmW, tmX, p, st);
     case 8: return launch_proj<8, EPI>(tmW, tmX, p, st);
     case 16: return launch_proj<16, EPI>(tmW, tmX, p, st);
     case 64: return launch_proj<64, EPI>(tmW, tmX, p, st);
@@ -972,7 +1238,44 @@ int choose_bm(int M) {
   return 128;
 }
 
+bool pair_rows(int M) {
+  // Measured on whole rounds at the 8B widths (B = 16..64, widths 2..16): the pair
+  // kernel is faster from 65 to 192 token rows (one tile), from 257 to 384 (two
+  // tiles of up to 192) and beyond 512; at 193..256 and 385..512 rows, where it
+  // would run tiles of more than 192 rows (three 32 KB stages per CTA), the
+  // single-CTA kernel's 128-row tiles are faster, and below 65 rows too.
+  return (M > 64 && M <= 192) || (M > 256 && M <= 384) || M > 512;
+}
+
+int pair_tile_rows(int M) {
+  // As few token tiles of at most 256 rows as possible -- each is one more pass of
+  // the weights through L2 -- unless tiles of at most 192 rows come to a multiple
+  // of four: the widest projection (gate/up, 112 weight pairs) then fills its
+  // waves of two CTAs per SM (4 tiles: 896 CTAs, 2.95 waves of 304; 3 tiles: 672,
+  // 2.2 waves).  Measured: 768 rows 13.4 ms in 4 tiles, 14.7 ms in 3.
+  const int n_wide = (M + kTc2MaxRows - 1) / kTc2MaxRows, n_narrow = (M + kTc2ChunkRows - 1) / kTc2ChunkRows;
+  const int ntt = (n_narrow % 4 == 0 && n_wide % 4 != 0) ? n_narrow : n_wide;
+  int T = ((M + ntt - 1) / ntt + 15) & ~15;
+  if (T > kTc2ChunkRows) T = (T + 31) & ~31;  // two epilogue chunks of a multiple of 16 rows
+  return T;
+}
+
 int choose_splits(int N, int K, int M, int BM, int sm_count, int max_splits) {
+  if (BM == kPairBM) {
+    // The most splits for which every tile's cluster of 2 x splits CTAs is resident
+    // in one wave (two CTAs per SM), with every split non-empty and at least 4
+    // k-blocks long.
+    const int T = pair_tile_rows(M);
+    const int pairs = (N / (2 * kBN)) * ((M + T - 1) / T);
+    const int kb = K / kBK;
+    const int smax = std::min({max_splits, kMaxSplits / 2, std::max(1, kb / 4), std::max(1, sm_count / pairs)});
+    for (int s = smax; s > 1; --s) {
+      const int per = (kb + s - 1) / s;
+      if ((kb + per - 1) / per != s) continue;  // some split would be empty
+      if (pairs <= max_active_clusters_bm(8, 2 * s)) return s;
+    }
+    return 1;
+  }
   // The most splits (cluster size) for which every tile's cluster is resident in
   // one wave (two CTAs per SM for every token tile; the GPC layout limits how
   // many clusters fit), with every split non-empty and at least 4 k-blocks long.
@@ -991,6 +1294,8 @@ int choose_splits(int N, int K, int M, int BM, int sm_count, int max_splits) {
 cudaError_t launch_gemm_epi(int epi, const CUtensorMap* tmW, const CUtensorMap* tmX, int BM, EpiParams p,
                             cudaStream_t st) {
   p.kb_total = p.K / kBK;
+  p.tok_tile = BM == kPairBM ? pair_tile_rows(p.M) : 0;
+  p.tok_chunk = p.tok_tile > kTc2ChunkRows ? p.tok_tile / 2 : p.tok_tile;
   p.kb_per_split = (p.kb_total + p.splits - 1) / p.splits;
   switch (epi) {
     case kEpiQKV: return launch_epi<kEpiQKV>(tmW, tmX, BM, p, st);

@@ -59,6 +59,8 @@ struct EpiParams {
   // kernel starts); split evenly over the CTAs.  Null / 0: none.
   const void* l2_next;
   unsigned long long l2_next_bytes;  // multiple of 16
+  int tok_tile;                      // token rows per tile (pair kernel; 0: the kernel's tile)
+  int tok_chunk;                     // token rows per epilogue chunk (pair kernel)
   int sm_count;
   // Set by the launcher: release the next kernel (programmatic dependent launch) only
   // as each CTA finishes, for grids of more than one wave.  Released early, the next
@@ -73,6 +75,12 @@ cudaError_t launch_gemm_epi(int epi, const CUtensorMap* tmW, const CUtensorMap* 
 // Choose split-K for an N x K projection over M rows so that the grid fills the GPU.
 int choose_splits(int N, int K, int M, int BM, int sm_count, int max_splits);
 int choose_bm(int M);
+// CTA-pair tcgen05 kernel (BM = kPairBM; every N a multiple of 256): whether it
+// serves M token rows, and its token tile (rows per tile, at most 256, a multiple
+// of 16; its X tensor map has boxes of pair_tile_rows(M) / 2 rows).
+constexpr int kPairBM = 256;
+bool pair_rows(int M);
+int pair_tile_rows(int M);
 
 // --- elementwise (elementwise.cu): resid = E[tok]; xn = fp16(E[tok] * g); ssq partials
 cudaError_t launch_embed(const int32_t* tok, int M, const __nv_bfloat16* embed, const float* gain, int d, int vocab,

@@ -1,8 +1,9 @@
 """GPU parity at the Llama-3.1-8B widths (d 4096, 32/8 heads of 128, ffn 14336,
 vocab 128256).  A 2-layer model is compared with the oracle element by element at
-row counts that take both projection paths (<= 16 rows: mma.sync; from 17 rows:
-tcgen05 in 64- or 128-row token tiles, 208-320 rows as two or three side by side,
-the last one ragged); the full 32-layer model, in the launch configuration the bench
+row counts that take every projection path (<= 16 rows: mma.sync; 17-64 rows and
+193-256 rows: single-CTA tcgen05 tiles of 64 or 128 rows; 65-192 and 257-384 rows:
+CTA-pair tcgen05 tiles, one or two of them, the last one ragged); the full 32-layer
+model, in the launch configuration the bench
 times (B = 1, 1024 cached tokens), is checked through properties that hold at any
 size and through the oracle's page allocator."""
 import numpy as np
@@ -48,8 +49,8 @@ def _prefill_both(dims, m, o, lens, seed, prompts=None):
     return ids, prompts
 
 
-@pytest.mark.parametrize("B,W", [(1, 1), (1, 5), (1, 8), (1, 16), (3, 7), (4, 16), (8, 12), (16, 13), (16, 16),
-                                 (20, 16)])
+@pytest.mark.parametrize("B,W", [(1, 1), (1, 5), (1, 8), (1, 16), (3, 7), (4, 16), (16, 5), (8, 12), (12, 16),
+                                 (16, 13), (16, 16), (20, 16)])
 def test_logits_match_oracle(two_layer, B, W):
     dims, w, m, o = two_layer
     lens = [70 + 7 * b for b in range(B)]              # ragged, across a page boundary
@@ -103,6 +104,43 @@ def test_greedy_verify_rounds_match_oracle(two_layer, margins):
         np.testing.assert_array_equal(np.array(pt), o.kv.page_table_array(ids))
     margins(compared, near)
     assert compared >= 8, (compared, near)
+
+
+@pytest.fixture(scope="module")
+def two_layer_wide():
+    need_gpu()
+    dims = synth.LLAMA8B.with_layers(2)
+    m = cuda_model(dims, {}, max_batch=64, max_width=16, max_seq_len=160, num_pages=64 * 3 + 8)
+    m.load_weights(synth.iter_weights(dims, seed=6, device="cuda", gain_jitter=0.1))
+    yield dims, m
+    m.close()
+
+
+@pytest.mark.parametrize("W", [10, 12, 16])
+def test_wide_batches_match_small_batches(two_layer_wide, W):
+    """64 sequences x W rows (640, 768, 1024 token rows: the CTA-pair tcgen05
+    projections in four token tiles of 160, 192 and 256 rows, the last in two
+    epilogue chunks) score what the same sequences score in batches of four (at
+    most 64 rows: the single-CTA tiles).  The two paths differ only in summation
+    order; a wrong tile, chunk or split shows up as an error of order one.  Scoring
+    the wide batch again gives the same bits."""
+    dims, m = two_layer_wide
+    B = 64
+    g = np.random.default_rng(40 + W)
+    lens = [40 + (7 * b) % 50 for b in range(B)]
+    ids = list(range(B))
+    m.seq_reset(ids)
+    prompts = torch.from_numpy(g.integers(0, dims.vocab, (B, max(lens)))).int()
+    m.prefill(ids, prompts.cuda(), lens)
+    tok = torch.from_numpy(np.concatenate([np.array([[int(prompts[b, lens[b] - 1])] for b in range(B)]),
+                                           g.integers(0, dims.vocab, (B, W - 1))], axis=1)).int().cuda()
+    wide = m.score(ids, tok).clone()
+    for b0 in (0, 28, 60):
+        small = m.score(ids[b0:b0 + 4], tok[b0:b0 + 4])
+        err = rel_err(wide[b0:b0 + 4].cpu().numpy(), small.cpu().numpy())
+        assert err < 5e-3, (W, b0, err)
+    for _ in range(3):
+        assert torch.equal(m.score(ids, tok), wide)
 
 
 @pytest.fixture(scope="module")
