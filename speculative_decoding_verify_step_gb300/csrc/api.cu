@@ -183,9 +183,12 @@ spec_status validate_cfg(const spec_config& c) {
 }
 
 // Bytes prefetched into L2 around a latency-bound attention launch (it runs ~9 us;
-// the prefetch also overlaps the O projection's start).  Measured optimum of
-// 34-120 MB at B = 1.
-constexpr double kAttnL2Budget = 90e6;
+// the prefetch also overlaps the O projection's start), after the QKV projection
+// has prefetched the O projection's weights: the start of gate/up.  Measured at
+// B = 1, width 5: 2.79 ms per round with O from the QKV projection and 45 MB here
+// (30-60 MB within 0.2%), 2.85 ms with 90 MB here (O and gate/up) and nothing from
+// the QKV projection, whose own weights arrive under the previous kernels.
+constexpr double kAttnL2Budget = 45e6;
 // Bytes of the next projection's weights prefetched into L2 at the end of each
 // projection's weight stream (HBM idles while its grid drains, ~2-3 us).  Only
 // while the projections are weight streams (mma.sync tiles, <= 16 token rows; measured: neutral
@@ -293,13 +296,16 @@ spec_status forward(spec_model* m, int B, int W, const int32_t* seq_ids, const i
   // While per-kernel profiling is on, no kernel prefetches another's weights: each
   // launch is then timed on the bytes it moves itself.
   const bool prefetch = !m->profiling;
-  const double pf = prefetch ? std::max(0.0, kAttnL2Budget - kv_bytes) : 0.0;
-  const unsigned long long pf_o = (unsigned long long)std::min(pf, wb_o) & ~15ull;
-  const unsigned long long pf_gu = (unsigned long long)std::max(0.0, std::min(pf - (double)pf_o, wb_gu)) & ~15ull;
   const double proj_pf = prefetch && BM <= 16 ? kProjL2Budget : 0.0;
+  // The QKV projection (mma.sync tiles) prefetches the O projection's weights; the
+  // attention, what is left of them and then the start of gate/up.
+  const unsigned long long q_o = prefetch && BM <= 16 ? (unsigned long long)wb_o & ~15ull : 0ull;
+  const double pf = prefetch ? std::max(0.0, kAttnL2Budget - kv_bytes) : 0.0;
+  const unsigned long long pf_o = (unsigned long long)std::min(pf, wb_o - (double)q_o) & ~15ull;
+  const unsigned long long pf_gu = (unsigned long long)std::max(0.0, std::min(pf - (double)pf_o, wb_gu)) & ~15ull;
   for (int l = 0; l < c.n_layers; ++l) {
     auto& Ly = m->layers[l];
-    ap.l2_next[0] = Ly.wo;
+    ap.l2_next[0] = reinterpret_cast<const char*>(Ly.wo) + q_o;
     ap.l2_next_bytes[0] = pf_o;
     ap.l2_next[1] = Ly.wgu;
     ap.l2_next_bytes[1] = pf_gu;
@@ -320,6 +326,8 @@ spec_status forward(spec_model* m, int B, int W, const int32_t* seq_ids, const i
       e.q_out = m->qrot;
       e.kpool = m->kpool + l * layer_elems;
       e.vpool = m->vpool + l * layer_elems;
+      e.l2_next = Ly.wo;
+      e.l2_next_bytes = q_o;
       CUDA_TRY(profiled(m, 0, wb_qkv, st, [&] { return launch_gemm_epi(kEpiQKV, &Ly.tm_qkv, tmx_xn, BM, e, st); }));
     }
     ap.layer_row0 = l * c.num_pages * Hkv * kPage;
@@ -337,7 +345,7 @@ spec_status forward(spec_model* m, int B, int W, const int32_t* seq_ids, const i
       e.ssq_out = m->ssq_b;
       e.d = d;
       e.l2_next = reinterpret_cast<const char*>(Ly.wgu) + pf_gu;
-      e.l2_next_bytes = (unsigned long long)std::min(proj_pf, wb_gu - (double)pf_gu) & ~15ull;
+      e.l2_next_bytes = (unsigned long long)std::max(0.0, std::min(proj_pf, wb_gu - (double)pf_gu)) & ~15ull;
       CUDA_TRY(profiled(m, 1, wb_o, st, [&] { return launch_gemm_epi(kEpiResid, &Ly.tm_o, tmx_attn, BM, e, st); }));
     }
     {
