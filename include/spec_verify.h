@@ -337,7 +337,11 @@ spec_status spec_kv_fill_random(spec_model* m, int32_t n, const int32_t* seq_ids
 spec_status spec_set_profiling(spec_model* m, int32_t enable);
 spec_status spec_read_profile(spec_model* m, double* ms, int64_t* launches, double* bytes);
 
-/* Synchronise `stream`, return and clear the device status word. */
+/* Synchronise `stream`, return and clear the device status word.
+ * SPEC_ERR_UNSUPPORTED reported from the device means a pair of CTAs of the
+ * tensor-core projection for 65+ token rows (which share one MMA across two SMs)
+ * was not placed on the two SMs of one TPC and computed nothing; the model then
+ * serves those row counts with single-CTA tiles from the next call on. */
 spec_status spec_sync_status(spec_model* m, void* stream);
 
 /* Pages per sequence in the page table (ceil(max_seq_len / page_size)). */

@@ -1266,6 +1266,10 @@ spec_status spec_sync_status(spec_model* m, void* stream) {
   std::vector<int32_t> lens(m->cfg.max_batch);
   CUDA_TRY(cudaMemcpy(lens.data(), m->seq_len, lens.size() * 4, cudaMemcpyDeviceToHost));
   for (size_t i = 0; i < lens.size(); ++i) m->host_len_bound[i] = std::max(0, (int)lens[i]);
+  // The only device-side SPEC_ERR_UNSUPPORTED: a CTA pair of the pair projection
+  // kernel not placed on the two SMs of one TPC (it computed nothing).  Later
+  // calls use the single-CTA tensor-core tiles instead.
+  if (code == SPEC_ERR_UNSUPPORTED) m->pair_ok = false;
   if (code != 0) return fail((spec_status)code, "device reported status %d", code);
   return SPEC_OK;
 }
