@@ -71,31 +71,37 @@ def test_logits_match_oracle(two_layer, B, W):
     assert rel_err(k.float().numpy(), kr) < TOL
 
 
-def test_greedy_verify_rounds_match_oracle(two_layer, margins):
+@pytest.mark.parametrize("B", [4, 16])
+def test_greedy_verify_rounds_match_oracle(two_layer, margins, B):
+    """Greedy verify rounds (width 5) against the oracle's decisions: 20 rows take the
+    single-CTA tensor-core tiles, 80 rows the CTA-pair kernel -- the LM head's
+    per-tile statistics that the acceptance reads included."""
     dims, w, m, o = two_layer
-    ids, prompts = _prefill_both(dims, m, o, [80, 66, 90, 71], seed=7)
+    ids, prompts = _prefill_both(dims, m, o, [80, 66, 90, 71] if B == 4 else [64 + (11 * b) % 37 for b in range(B)],
+                                 seed=7)
     gamma = 4
     hist = [list(map(int, p)) for p in prompts]
     compared = near = 0
-    for r in range(4):
-        tok = np.zeros((4, gamma + 1), np.int64)
+    for r in range(4 if B == 4 else 3):
+        tok = np.zeros((B, gamma + 1), np.int64)
         tok[:, 0] = [h[-1] for h in hist]
         for i in range(1, gamma + 1):                 # drafts = the oracle's greedy continuation
             tok[:, i] = o.forward(ids, tok[:, :i])[:, i - 1].argmax(-1)
-        tok[r % 4, 1 + r] = (tok[r % 4, 1 + r] + 1) % dims.vocab   # one wrong draft per round
+        for b in range(r % 4, B, 4):                  # one wrong draft in a quarter of the sequences
+            tok[b, 1 + r] = (tok[b, 1 + r] + 1) % dims.vocab
         ref = o.forward(ids, tok)
         n_ref, com_ref, _ = A.accept_greedy(ref, tok[:, 1:])
         acc, com, _ = m.verify_step(ids, torch.from_numpy(tok).cuda())
         acc, com = acc.cpu().numpy(), com.cpu().numpy()
         gap = top2_gap(ref)
-        for b in range(4):
+        for b in range(B):
             if (gap[b, :n_ref[b] + 1] > 1e-2).all():
                 compared += 1
                 assert acc[b] == n_ref[b] and (com[b] == com_ref[b]).all()
             else:
                 near += 1
         o.commit(ids, n_ref, gamma + 1)
-        for b in range(4):
+        for b in range(B):
             hist[b].extend(int(t) for t in com_ref[b, :n_ref[b] + 1])
         if not ((acc == n_ref).all() and (com == com_ref).all()):   # restart both from the oracle's history
             ids, _ = _prefill_both(dims, m, o, [len(h) for h in hist], seed=0, prompts=hist)
