@@ -125,6 +125,7 @@ struct spec_model {
   int32_t *row_pos = nullptr, *row_slot = nullptr, *seq_start = nullptr;
   int32_t *seq_wlen = nullptr, *seq_rowoff = nullptr;  // per-call window layout (prepare kernel)
   int32_t* seq_ok = nullptr;  // per-call: 1 = the window got its pages and may commit
+  int32_t* seq_order = nullptr;  // per-call: batch indices by cached length, longest first
   float *rope_cos = nullptr, *rope_sin = nullptr;
   int32_t *scratch_ids = nullptr, *scratch_ids2 = nullptr, *scratch_tok = nullptr, *scratch_lens = nullptr;
   int32_t *scratch_acc = nullptr, *scratch_bonus = nullptr;
@@ -238,6 +239,7 @@ spec_status forward(spec_model* m, int B, int W, const int32_t* seq_ids, const i
   pp.row_slot = m->row_slot;
   pp.seq_start = m->seq_start;
   pp.seq_ok = m->seq_ok;
+  pp.seq_order = m->seq_order;
   pp.tok = tok;
   pp.vocab = c.vocab;
   pp.status = m->status;
@@ -271,6 +273,7 @@ spec_status forward(spec_model* m, int B, int W, const int32_t* seq_ids, const i
   ap.seq_start = m->seq_start;
   ap.seq_wlen = m->seq_wlen;
   ap.seq_rowoff = m->seq_rowoff;
+  ap.seq_order = m->seq_order;
   ap.max_pages = m->max_pages;
   ap.max_batch = c.max_batch;
   ap.B = B;
@@ -619,6 +622,7 @@ spec_status spec_model_create(const spec_config* cfg, spec_model** out) {
   ALLOC(m->seq_wlen, c.max_batch);
   ALLOC(m->seq_rowoff, c.max_batch);
   ALLOC(m->seq_ok, c.max_batch);
+  ALLOC(m->seq_order, c.max_batch);
   ALLOC(m->rope_cos, (size_t)c.max_seq_len * (hd / 2));
   ALLOC(m->rope_sin, (size_t)c.max_seq_len * (hd / 2));
   ALLOC(m->scratch_ids, c.max_batch);

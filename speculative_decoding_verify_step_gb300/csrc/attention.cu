@@ -87,7 +87,7 @@ __global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32)
 
   const int rank = (int)cluster.block_rank();  // == blockIdx.x: the split of this CTA
   const int kvh = blockIdx.y;
-  const int b = blockIdx.z;
+  const int b = p.seq_order ? p.seq_order[blockIdx.z] : blockIdx.z;  // longest cache first
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n_cons = blockDim.x / 32 - 1;  // consumer warps: (row tile, key group) pairs

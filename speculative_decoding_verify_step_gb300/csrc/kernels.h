@@ -97,6 +97,7 @@ struct AttnParams {
   const int32_t* seq_start;    // [B] cached length L at round start
   const int32_t* seq_wlen;     // [B] window rows of sequence b
   const int32_t* seq_rowoff;   // [B] first flat row of sequence b
+  const int32_t* seq_order;    // [B] batch index of the z-th CTA group (longest cache first)
   int max_pages, max_batch;
   int B, W, Hq, Hkv, hd;       // W: the widest window of the call
   int layer_row0;              // first TMA row of this layer in the KV pool maps
@@ -132,6 +133,7 @@ struct PrepareParams {
   int32_t* row_slot;        // [B*W] physical slot (page*64 + off) or -1
   int32_t* seq_start;       // [B]
   int32_t* seq_ok;          // [B] out: 1 = the window got its pages and may commit
+  int32_t* seq_order;       // [B] out: batch indices by cached length, longest first
   const int32_t* tok;       // [B*W] token ids to validate
   int vocab;
   int* status;

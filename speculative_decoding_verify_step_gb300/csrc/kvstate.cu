@@ -86,6 +86,23 @@ __global__ void __launch_bounds__(32) prepare_kernel(const __grid_constant__ Pre
     __syncwarp();
   }
   if (lane == 0 && off != p.total_rows) set_status(p.status, SPEC_ERR_INVALID_ARG);
+  // The attention's CTA groups go longest cache first: with more groups than one
+  // wave, the short ones fill in behind the long ones instead of a long one
+  // starting last.  Rank of b: the sequences with a longer cache, or an equal one
+  // and a lower index (a permutation).  Up to 256 sequences; beyond, batch order.
+  __syncwarp();
+  for (int b = lane; b < p.B; b += 32) {
+    int r = b;
+    if (p.B <= 256) {
+      const int Lb = p.seq_start[b];
+      r = 0;
+      for (int j = 0; j < p.B; ++j) {
+        const int Lj = p.seq_start[j];
+        r += (Lj > Lb || (Lj == Lb && j < b)) ? 1 : 0;
+      }
+    }
+    p.seq_order[r] = b;
+  }
 }
 
 __global__ void seq_reset_kernel(const int32_t* seq_ids, int n, int32_t* seq_len, int32_t* seq_npages,
