@@ -244,7 +244,7 @@ SPEC_DEVICE_INLINE void finish_tile(const EpiParams& p, const EpiPre<EPI, NT, RO
     cluster_arrive();  // done reading the other CTAs' tiles
   }
   // weight-row scale 2^-e of the fp16 encoding, per output column of the tile
-  __shared__ float s_rs_own[kBN];
+  __shared__ __align__(16) float s_rs_own[kBN];
   float* s_rs = PREP ? s_rs_prep : s_rs_own;
   // per-row scale of a normalised input: s_m = rsqrt(sum_t ssq[t][m] / d + eps).
   // One warp per row, tiles lane, lane + 32, ... per lane (then a fixed shuffle
@@ -321,31 +321,37 @@ SPEC_DEVICE_INLINE void finish_tile(const EpiParams& p, const EpiPre<EPI, NT, RO
       }
     };
     if constexpr (PREP) {
-      // four consecutive pairs (i .. i+3 of one head) per item, eight items per
+      // four consecutive pairs (i .. i+3 of one head) per item, two items per
       // thread at a time: their angles are loaded together, then written as
-      // 8-byte groups
+      // 8-byte groups (measured, 80-row tiles: batches of two finish the tile in
+      // half the time of batches of eight, with the same loads)
+      // head_dim is 64 or 128 and the tile starts on a head boundary (n0 is a
+      // multiple of 128): pair pr of a row is element i = pr mod hd/2 of head
+      // n0/hd + pr div hd/2, the divisions done as shifts and masks
+      const int lh = 31 - __clz(p.hd);
+      const int hmask = half - 1;
+      const int head0 = n0 >> lh;
       const int n_quads = n_pairs / 4;
-      constexpr int kB = 8;
+      constexpr int kB = 2;
       for (int e0 = tid; e0 < n_quads; e0 += kB * NT) {
         float4 cs[kB], sn[kB];
 #pragma unroll
         for (int j = 0; j < kB; ++j) {
-          const int e = min(e0 + j * NT, n_quads - 1);
-          const int ml = r_lo + e / (kBN / 8), pr = (e % (kBN / 8)) * 4;
-          const int i = (n0 + (pr / half) * p.hd + pr % half) % p.hd;
-          const long long a = (long long)s_ps[ml].x * half + i;
+          const unsigned e = (unsigned)min(e0 + j * NT, n_quads - 1);
+          const int ml = r_lo + (int)(e / (kBN / 8)), pr = (int)(e % (kBN / 8)) * 4;
+          const long long a = (long long)s_ps[ml].x * half + (pr & hmask);
           cs[j] = __ldg(reinterpret_cast<const float4*>(p.rope_cos + a));
           sn[j] = __ldg(reinterpret_cast<const float4*>(p.rope_sin + a));
         }
 #pragma unroll
         for (int j = 0; j < kB; ++j) {
-          const int e = e0 + j * NT;
-          if (e >= n_quads) break;
-          const int ml = r_lo + e / (kBN / 8), pr = (e % (kBN / 8)) * 4;
+          const unsigned e = (unsigned)(e0 + j * NT);
+          if (e >= (unsigned)n_quads) break;
+          const int ml = r_lo + (int)(e / (kBN / 8)), pr = (int)(e % (kBN / 8)) * 4;
           const int m = m0 + ml;
-          const int cl = (pr / half) * p.hd + pr % half;
-          const int n = n0 + cl;
-          const int head = n / p.hd, i = n % p.hd;
+          const int hl = pr >> (lh - 1), i = pr & hmask;
+          const int cl = (hl << lh) + i;
+          const int head = head0 + hl;
           const float sc = s_scale[ml];
           const float4 ta = *reinterpret_cast<const float4*>(&tile[ml * kTilePad + cl]);
           const float4 tb = *reinterpret_cast<const float4*>(&tile[ml * kTilePad + cl + half]);
@@ -368,11 +374,11 @@ SPEC_DEVICE_INLINE void finish_tile(const EpiParams& p, const EpiPre<EPI, NT, RO
           if (head < p.Hq) {
             dst = p.q_out + ((long long)m * p.Hq + head) * p.hd;
           } else if (s_ps[ml].y >= 0) {  // slot < 0: the round failed to get a page for this row
-            const int slot = s_ps[ml].y;
+            const unsigned slot = (unsigned)s_ps[ml].y;
             const bool is_k = head < p.Hq + p.Hkv;
             const int kvh = is_k ? head - p.Hq : head - p.Hq - p.Hkv;
             dst = (is_k ? p.kpool : p.vpool) +
-                  (((long long)(slot / kPage) * p.Hkv + kvh) * kPage + slot % kPage) * p.hd;
+                  ((((long long)(slot / kPage) * p.Hkv + kvh) * kPage + slot % kPage) << lh);
           }
           if (dst) {
             *reinterpret_cast<uint2*>(dst + i) = pack_act4(av[0], av[1], av[2], av[3]);
@@ -413,16 +419,24 @@ SPEC_DEVICE_INLINE void finish_tile(const EpiParams& p, const EpiPre<EPI, NT, RO
       }
     }
   } else if constexpr (EPI == kEpiSwiGLU) {
-    // tile = 64 gate rows then the 64 up rows of the same features
+    // tile = 64 gate rows then the 64 up rows of the same features; four
+    // consecutive features of one row per item (16-byte tile reads, 8-byte stores)
     const int f0 = (n0 / kBN) * 64;
-    for (int e = tid; e < max(0, r_hi - r_lo) * 64; e += NT) {
-      const int ml = r_lo + e / 64, fl = e % 64;
+    const unsigned n_items = max(0, r_hi - r_lo) * 16;
+    for (unsigned e = tid; e < n_items; e += NT) {
+      const int ml = r_lo + (int)(e / 16), fl = (int)(e % 16) * 4;
       const int m = m0 + ml;
       const float sc = s_scale[ml];
-      const float gv = tile[ml * kTilePad + fl] * (sc * s_rs[fl]);
-      const float uv = tile[ml * kTilePad + 64 + fl] * (sc * s_rs[64 + fl]);
-      const float silu = gv / (1.f + expf(-gv));
-      p.act[(long long)m * p.ffn + f0 + fl] = to_act(silu * uv);
+      const float4 tg = *reinterpret_cast<const float4*>(&tile[ml * kTilePad + fl]);
+      const float4 tu = *reinterpret_cast<const float4*>(&tile[ml * kTilePad + 64 + fl]);
+      const float4 rg = *reinterpret_cast<const float4*>(&s_rs[fl]);
+      const float4 ru = *reinterpret_cast<const float4*>(&s_rs[64 + fl]);
+      const float g4[4] = {tg.x * (sc * rg.x), tg.y * (sc * rg.y), tg.z * (sc * rg.z), tg.w * (sc * rg.w)};
+      const float u4[4] = {tu.x * (sc * ru.x), tu.y * (sc * ru.y), tu.z * (sc * ru.z), tu.w * (sc * ru.w)};
+      float h[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) h[k] = g4[k] / (1.f + expf(-g4[k])) * u4[k];
+      *reinterpret_cast<uint2*>(p.act + (long long)m * p.ffn + f0 + fl) = pack_act4(h[0], h[1], h[2], h[3]);
     }
   } else if constexpr (EPI == kEpiResid) {
     // r += y; next input X' = fp16(r * g_next); per-tile sum of r^2 for the next norm.
@@ -717,8 +731,23 @@ SPEC_DEVICE_INLINE void tc_prep(const EpiParams& p, int m0, int n0, float* s_sca
       if (r < r_hi && lane == 0) s_scale[r] = p.ssq_in ? rsqrtf(sum * p.inv_d + p.eps) : 1.f;
     }
   }
-  if constexpr (EPI == kEpiQKV)
-    for (int r = r_lo + t; r < r_hi; r += 128) s_ps[r] = make_int2(__ldcg(p.row_pos + m0 + r), __ldcg(p.row_slot + m0 + r));
+  // The epilogue's other inputs are read from memory once the accumulator is
+  // ready; by then the weight stream (and, before O, the KV cache) has usually
+  // pushed them out of L2, so they are brought back into L2 now: each row's RoPE
+  // angles (QKV tiles of rotated heads) or residual segment (O and down).
+  if constexpr (EPI == kEpiQKV) {
+    const bool rotated = n0 / p.hd < p.Hq + p.Hkv;
+    for (int r = r_lo + t; r < r_hi; r += 128) {
+      const int pos = __ldcg(p.row_pos + m0 + r);
+      s_ps[r] = make_int2(pos, __ldcg(p.row_slot + m0 + r));
+      if (rotated) {
+        l2_prefetch_bulk(p.rope_cos + (long long)pos * (p.hd >> 1), (uint32_t)p.hd * 2);
+        l2_prefetch_bulk(p.rope_sin + (long long)pos * (p.hd >> 1), (uint32_t)p.hd * 2);
+      }
+    }
+  }
+  if constexpr (EPI == kEpiResid)
+    for (int r = r_lo + t; r < r_hi; r += 128) l2_prefetch_bulk(p.resid + (long long)(m0 + r) * p.d + n0, kBN * 4);
 }
 
 template <int NT, int EPI>
