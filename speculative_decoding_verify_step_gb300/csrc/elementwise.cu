@@ -18,8 +18,11 @@ __global__ void __launch_bounds__(kTileCols) embed_kernel(const int32_t* tok, co
                                                           act_t* xn, float* ssq_out, int ssq_stride,
                                                           int* status) {
   __shared__ float red[kTileCols / 32];
-  pdl_wait();
+  // The first projection may start streaming its weights now: it reads nothing of
+  // this kernel's (or the round preparation's) output before its own dependency
+  // wait, which returns once this grid, and so the preparation before it, is done.
   pdl_launch_dependents();
+  pdl_wait();
   const int m = blockIdx.x;
   const int col = blockIdx.y * kTileCols + threadIdx.x;
   int t = tok[m];

@@ -9,23 +9,38 @@ namespace spec {
 
 namespace {
 
-// One warp.  Sequences are served in batch order b = 0..B-1 (deterministic page
-// assignment).  Sequence b owns flat rows rowoff_b .. rowoff_b + W_b - 1; for its
-// window row j: position L + depth[j] (RoPE), KV slot L + j.
+// One warp.  Sequence b owns flat rows rowoff_b .. rowoff_b + W_b - 1; for its
+// window row j: position L + depth[j] (RoPE), KV slot L + j.  Lengths, offsets,
+// positions, the slots of windows whose pages already exist and the token checks
+// are computed 32 sequences at a time; only the sequences that need new pages are
+// then served one at a time, in batch order b = 0..B-1 (deterministic page
+// assignment: the lowest free page first, as if every sequence were served in
+// turn -- the others take no page).
 //
 // A batch that names a sequence id out of range, or the same id twice, is refused
 // as a whole (SPEC_ERR_INVALID_ARG): no page is taken, no KV slot is given out and
 // every seq_ok[b] is 0, so the commit leaves every sequence as it was (two windows
 // of one sequence would write the same slots and race on its length and pages).
 // A sequence whose window cannot get its pages (SPEC_ERR_CAPACITY) gives back the
-// pages this call took for it and gets seq_ok[b] = 0.
-constexpr int kMaxBatchWords = 4096 / 32;  // max_batch <= 4096
+// pages this call took for it and gets seq_ok[b] = 0.  The status word keeps the
+// first error in batch order (per sequence: a refused window length, then a
+// capacity failure, then a token id out of range).
+constexpr int kMaxBatch = 4096;  // max_batch <= 4096 (checked by the launcher)
+constexpr int kMaxBatchWords = kMaxBatch / 32;
+constexpr int kRankMax = 256;    // sequences ranked by cached length (more: batch order)
+constexpr uint8_t kErrRefused = 1, kErrCapacity = 2, kErrToken = 4;
 __global__ void __launch_bounds__(32) prepare_kernel(const __grid_constant__ PrepareParams p) {
   __shared__ uint32_t s_seen[kMaxBatchWords];
+  __shared__ uint32_t s_alloc[kMaxBatchWords];  // bit b: sequence b needs pages this call
+  __shared__ uint8_t s_err[kMaxBatch];          // kErr* bits of sequence b
+  __shared__ int s_len[kRankMax];
   pdl_wait();
   pdl_launch_dependents();
   const int lane = threadIdx.x;
-  for (int i = lane; i < kMaxBatchWords; i += 32) s_seen[i] = 0u;
+  for (int i = lane; i < kMaxBatchWords; i += 32) {
+    s_seen[i] = 0u;
+    s_alloc[i] = 0u;
+  }
   __syncwarp();
   bool bad_ids = false;
   for (int b0 = 0; b0 < p.B; b0 += 32) {
@@ -43,61 +58,125 @@ __global__ void __launch_bounds__(32) prepare_kernel(const __grid_constant__ Pre
     bad_ids |= __any_sync(0xffffffffu, bad);
   }
   if (bad_ids && lane == 0) set_status(p.status, SPEC_ERR_INVALID_ARG);
-  int off = 0;
-  for (int b = 0; b < p.B; ++b) {
-    const int s = p.seq_ids[b];
-    int Wb = p.wlen ? p.wlen[b] : p.W;
-    if (Wb < 1 || Wb > p.W || off + Wb > p.total_rows) {  // refused, keeps every index in bounds
-      if (lane == 0) set_status(p.status, SPEC_ERR_INVALID_ARG);
-      Wb = max(0, min(min(Wb, p.W), p.total_rows - off));
+
+  // Sequences b0 .. b0+31, one per lane.  Window lengths are clamped to [0, W] and
+  // to the rows left (a length outside 1..W, or past total_rows, is refused), so the
+  // row offset of b is min(total_rows, sum of the clamped lengths before it): an
+  // exclusive prefix sum over the warp, carried from group to group.
+  int rows_before = 0;
+  for (int b0 = 0; b0 < p.B; b0 += 32) {
+    const int b = b0 + lane;
+    const bool in = b < p.B;
+    const int s = in ? p.seq_ids[b] : -1;
+    const int w_req = in ? (p.wlen ? p.wlen[b] : p.W) : 0;
+    const int c = max(0, min(w_req, p.W));
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
     }
-    const bool sid_ok = s >= 0 && s < p.max_batch;
+    const int off = min(p.total_rows, rows_before + incl - c);
+    rows_before = min(p.total_rows, rows_before + __shfl_sync(0xffffffffu, incl, 31));
+    const int Wb = max(0, min(c, p.total_rows - off));
+    uint8_t err = 0;
+    if (in && (w_req < 1 || w_req > p.W || off + w_req > p.total_rows)) err |= kErrRefused;
+    const bool sid_ok = in && s >= 0 && s < p.max_batch;
     const int L = sid_ok ? p.seq_len[s] : 0;
     bool ok = sid_ok && !bad_ids;
+    bool alloc = false;
     if (ok) {
-      if (L + Wb > p.max_seq_len) {
+      const int need = (L + Wb + kPage - 1) / kPage;
+      if (L + Wb > p.max_seq_len || need > p.max_pages) {
         ok = false;
+        err |= kErrCapacity;
       } else {
-        const int npg0 = p.seq_npages[s];
-        ok = warp_ensure_pages(s, L + Wb, p.seq_npages, p.page_table, p.max_pages, p.free_bits, p.num_pages);
-        if (!ok && lane == 0) release_pages_from(s, npg0, p.seq_npages, p.page_table, p.max_pages, p.free_bits);
+        alloc = need > p.seq_npages[s];  // pages are taken below, in batch order
       }
-      if (!ok && lane == 0) set_status(p.status, SPEC_ERR_CAPACITY);
     }
-    if (lane == 0) {
+    if (in) {
       p.seq_start[b] = L;
       p.seq_wlen[b] = Wb;
       p.seq_rowoff[b] = off;
       p.seq_ok[b] = ok ? 1 : 0;
-    }
-    for (int j = lane; j < Wb; j += 32) {
-      const int m = off + j;
-      p.row_pos[m] = min(L + p.depth[j], p.max_seq_len - 1);
-      int slot = -1;
-      if (ok) {
-        const int t = L + j;
-        slot = p.page_table[(long long)s * p.max_pages + t / kPage] * kPage + t % kPage;
+      for (int j = 0; j < Wb; ++j) {
+        const int m = off + j;
+        p.row_pos[m] = min(L + p.depth[j], p.max_seq_len - 1);
+        int slot = -1;
+        if (ok && !alloc) {
+          const int t = L + j;
+          slot = p.page_table[(long long)s * p.max_pages + t / kPage] * kPage + t % kPage;
+        }
+        p.row_slot[m] = slot;
+        const int tk = p.tok[m];
+        if (tk < 0 || tk >= p.vocab) err |= kErrToken;
       }
-      p.row_slot[m] = slot;
-      const int tk = p.tok[m];
-      if (tk < 0 || tk >= p.vocab) set_status(p.status, SPEC_ERR_INVALID_ARG);
+      s_err[b] = err;
     }
-    off += Wb;
-    __syncwarp();
+    const unsigned alloc_bits = __ballot_sync(0xffffffffu, alloc);
+    if (lane == 0) s_alloc[b0 >> 5] = alloc_bits;
   }
-  if (lane == 0 && off != p.total_rows) set_status(p.status, SPEC_ERR_INVALID_ARG);
+  __syncwarp();
+
+  // The sequences that need pages, in batch order (the whole warp serves each).
+  const int n_words = (p.B + 31) >> 5;
+  for (int w = 0; w < n_words; ++w) {
+    uint32_t bits = s_alloc[w];
+    while (bits) {
+      const int b = (w << 5) + __ffs(bits) - 1;
+      bits &= bits - 1u;
+      const int s = p.seq_ids[b];
+      const int L = p.seq_start[b], Wb = p.seq_wlen[b], off = p.seq_rowoff[b];
+      const int npg0 = p.seq_npages[s];
+      const bool ok = warp_ensure_pages(s, L + Wb, p.seq_npages, p.page_table, p.max_pages, p.free_bits, p.num_pages);
+      if (lane == 0) {
+        if (!ok) {
+          release_pages_from(s, npg0, p.seq_npages, p.page_table, p.max_pages, p.free_bits);
+          s_err[b] |= kErrCapacity;
+        }
+        p.seq_ok[b] = ok ? 1 : 0;
+      }
+      if (ok) {
+        for (int j = lane; j < Wb; j += 32) {
+          const int t = L + j;
+          p.row_slot[off + j] = p.page_table[(long long)s * p.max_pages + t / kPage] * kPage + t % kPage;
+        }
+      }
+      __syncwarp();
+    }
+  }
+
+  // The first error in batch order.
+  for (int b0 = 0; b0 < p.B; b0 += 32) {
+    const int b = b0 + lane;
+    const int e = b < p.B ? s_err[b] : 0;
+    const int code = (e & kErrRefused)    ? SPEC_ERR_INVALID_ARG
+                     : (e & kErrCapacity) ? SPEC_ERR_CAPACITY
+                     : (e & kErrToken)    ? SPEC_ERR_INVALID_ARG
+                                          : 0;
+    const unsigned any = __ballot_sync(0xffffffffu, code != 0);
+    if (any) {
+      if (lane == __ffs(any) - 1) set_status(p.status, code);
+      break;
+    }
+  }
+  if (lane == 0 && rows_before != p.total_rows) set_status(p.status, SPEC_ERR_INVALID_ARG);
+
   // The attention's CTA groups go longest cache first: with more groups than one
   // wave, the short ones fill in behind the long ones instead of a long one
   // starting last.  Rank of b: the sequences with a longer cache, or an equal one
-  // and a lower index (a permutation).  Up to 256 sequences; beyond, batch order.
+  // and a lower index (a permutation).  Up to kRankMax sequences; beyond, batch order.
+  const bool rank = p.B <= kRankMax;
+  if (rank)
+    for (int b = lane; b < p.B; b += 32) s_len[b] = p.seq_start[b];
   __syncwarp();
   for (int b = lane; b < p.B; b += 32) {
     int r = b;
-    if (p.B <= 256) {
-      const int Lb = p.seq_start[b];
+    if (rank) {
+      const int Lb = s_len[b];
       r = 0;
       for (int j = 0; j < p.B; ++j) {
-        const int Lj = p.seq_start[j];
+        const int Lj = s_len[j];
         r += (Lj > Lb || (Lj == Lb && j < b)) ? 1 : 0;
       }
     }
@@ -262,6 +341,7 @@ cudaError_t launch_init_state(int32_t* seq_len, int32_t* seq_npages, int32_t* pa
 }
 
 cudaError_t launch_prepare(const PrepareParams& p, cudaStream_t st) {
+  if (p.B < 1 || p.B > kMaxBatch || p.W < 1 || p.W > 16) return cudaErrorInvalidValue;
   return launch_k(prepare_kernel, dim3(1), dim3(32), 0, st, p);
 }
 
