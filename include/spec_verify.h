@@ -32,7 +32,11 @@
  *     bounded wait that ran out) set a device status word: the call that
  *     enqueued the work still returns SPEC_OK, and the next spec_sync_status()
  *     returns the code (and clears it).  Kernels that hit such an error skip the
- *     offending memory accesses, so the context stays usable.
+ *     offending memory accesses, so the context stays usable.  With several
+ *     errors the word keeps the first one set; within one round's preparation
+ *     that is the first in batch order (per sequence: a verify length outside
+ *     1..gamma+1, then a window that cannot get its pages, then a token id out
+ *     of range).
  *   - A sampled (temperature > 0) round with q or u missing is an error; the
  *     library never falls back to greedy.
  *   - seq_ids of one call must be distinct and in 0..max_batch-1.  A call that

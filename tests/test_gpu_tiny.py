@@ -406,6 +406,33 @@ def test_verify_round_on_an_exhausted_pool_keeps_the_length(tiny):
         m.close()
 
 
+def test_first_error_of_a_round_is_reported_in_batch_order(tiny):
+    """Two device-side errors in one round: the status word keeps the first in batch
+    order -- a sequence that cannot get its page (SPEC_ERR_CAPACITY) listed before a
+    sequence whose verify length exceeds the width (SPEC_ERR_INVALID_ARG), and the
+    other way round; the sequence without its page keeps its length either way."""
+    need_gpu()
+    from speculative_decoding_verify_step_gb300 import spec
+    w, _ = tiny
+    m = cuda_model(synth.TINY, w, max_batch=3, max_width=8, max_seq_len=256, num_pages=3)
+    try:
+        m.seq_reset([0, 1, 2])
+        m.prefill([0, 1], torch.zeros(2, 65, dtype=torch.int32).cuda(), [65, 64])  # 64 and 63 cached: pages 0, 1
+        m.prefill([2], torch.zeros(1, 30, dtype=torch.int32).cuda(), [30])         # page 2: the pool is full
+        m.sync_status()
+        before = m.kv_state([0])
+        tok = torch.ones(14, dtype=torch.int32).cuda()  # 5 + 9 rows, packed
+        # sequence 0 needs a second page (64 + 5 slots); sequence 2 asks for 9 rows of 8
+        for ids, lens, first in (([0, 2], [5, 9], 4), ([2, 0], [9, 5], 1)):
+            m.verify_ragged(ids, tok, lens, spec.RAGGED_COMPACT, gamma=7)
+            with pytest.raises(spec.SpecError) as e:
+                m.sync_status()
+            assert e.value.status == first, (ids, lens)
+            assert m.kv_state([0]) == before
+    finally:
+        m.close()
+
+
 def test_kv_write_gives_a_sequence_the_callers_cache(tiny):
     """spec_kv_write: the values read back bit for bit, pages taken lowest first, the
     length set; an exhausted pool reports SPEC_ERR_CAPACITY; wrong shapes are refused."""
